@@ -1,0 +1,177 @@
+"""Plain fp64 definition of exact attention, forward and backward (test infrastructure).
+
+Forward, per (batch, head), from "Flash Attention 原理与实践" §1.3 and
+"FlashAttention 与显存" §04:
+
+    S = scale * Q K^T                       [N, N]
+    causal: S_ij = -inf for j > i           (top-left aligned square mask, the
+                                             ``is_causal=True`` of the SDPA call shown in
+                                             "Flash Attention 原理与实践" §4.2)
+    m_i = max_j S_ij,  l_i = sum_j exp(S_ij - m_i)
+    P = exp(S - m) / l
+    O = P V
+    LSE_i = m_i + ln l_i                    (natural log, in units of scaled scores; the
+                                             one-number form of the (m, l) pair that
+                                             "FlashAttention 与显存" §09 keeps per row)
+
+Backward (analytic; "FlashAttention 与显存" §09 says only that S and P are recomputed
+from Q, K, V block by block).  With dO the upstream gradient of O:
+
+    dV = P^T dO
+    dP = dO V^T
+    D_i = sum_c dO_ic O_ic                  (equals sum_j P_ij dP_ij)
+    dS = P * (dP - D 1^T)
+    dQ = scale * dS K
+    dK = scale * dS^T Q
+
+S and P are materialised for a chunk of query rows at a time, over the full key
+length, which is still the plain definition (no online rescaling), and keeps the
+memory bounded for N = 65536.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+
+__all__ = [
+    "bf16_bits_to_f64",
+    "scores",
+    "attention_fwd",
+    "attention_fwd_rows",
+    "attention_bwd",
+    "attention_bwd_head",
+    "attention_bwd_rows",
+]
+
+
+def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
+    """Widen bfloat16 bit patterns (uint16) to float64 exactly.
+
+    A bfloat16 value is the upper half of the float32 with the same bits, so the
+    widening is a 16-bit shift into a float32 followed by an exact float64 cast.
+    """
+    bits = np.asarray(bits)
+    if bits.dtype != np.uint16:
+        raise TypeError("expected uint16 bfloat16 bit patterns")
+    return (bits.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
+
+
+def scores(q_rows: np.ndarray, k: np.ndarray, scale: float, causal: bool,
+           row_index: np.ndarray) -> np.ndarray:
+    """S rows for the queries whose positions are ``row_index``: scale * q k^T, masked.
+
+    q_rows: [R, d] fp64, k: [N, d] fp64, row_index: [R] int positions of the rows.
+    Masked entries are -inf.
+    """
+    s = scale * (q_rows @ k.T)
+    if causal:
+        n = k.shape[0]
+        key = np.arange(n)[None, :]
+        s = np.where(key > np.asarray(row_index)[:, None], -np.inf, s)
+    return s
+
+
+def _softmax_rows(s: np.ndarray):
+    m = s.max(axis=1)
+    e = np.exp(s - m[:, None])
+    l = e.sum(axis=1)
+    return e / l[:, None], m, l
+
+
+def attention_fwd(q, k, v, scale: float, causal: bool, row_chunk: int = 512):
+    """O [B,H,N,d] and LSE [B,H,N] in fp64 for fp64 inputs [B,H,N,d]."""
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    B, H, N, d = q.shape
+    o = np.empty((B, H, N, v.shape[-1]))
+    lse = np.empty((B, H, N))
+    for b in range(B):
+        for h in range(H):
+            for r0 in range(0, N, row_chunk):
+                r1 = min(N, r0 + row_chunk)
+                rows = np.arange(r0, r1)
+                s = scores(q[b, h, r0:r1], k[b, h], scale, causal, rows)
+                p, m, l = _softmax_rows(s)
+                o[b, h, r0:r1] = p @ v[b, h]
+                lse[b, h, r0:r1] = m + np.log(l)
+    return o, lse
+
+
+def attention_fwd_rows(q_head, k_head, v_head, scale: float, causal: bool, rows):
+    """O and LSE for selected query rows of one head.
+
+    q_head, k_head, v_head: [N, d] fp64 for one (batch, head); rows: positions.
+    Each row of attention depends only on its own query and all keys, so a sample of
+    rows is checked against the same definition as the whole tensor.
+    """
+    rows = np.asarray(rows, dtype=np.int64)
+    s = scores(np.asarray(q_head, np.float64)[rows], np.asarray(k_head, np.float64),
+               scale, causal, rows)
+    p, m, l = _softmax_rows(s)
+    return p @ np.asarray(v_head, np.float64), m + np.log(l)
+
+
+def attention_bwd_head(q, k, v, do, scale: float, causal: bool, row_chunk: int = 512):
+    """dQ, dK, dV [N, d] and D [N] for one head, all fp64 [N, d] inputs.
+
+    D is rowsum(dO * O) with O from this same definition.
+    """
+    q = np.asarray(q, np.float64)
+    k = np.asarray(k, np.float64)
+    v = np.asarray(v, np.float64)
+    do = np.asarray(do, np.float64)
+    N = q.shape[0]
+    dq = np.empty_like(q)
+    dk = np.zeros_like(k)
+    dv = np.zeros_like(v)
+    dvec = np.empty(N)
+    for r0 in range(0, N, row_chunk):
+        r1 = min(N, r0 + row_chunk)
+        rows = np.arange(r0, r1)
+        s = scores(q[r0:r1], k, scale, causal, rows)
+        p, _, _ = _softmax_rows(s)
+        o = p @ v
+        dv += p.T @ do[r0:r1]
+        dp = do[r0:r1] @ v.T
+        drow = np.sum(do[r0:r1] * o, axis=1)
+        ds = p * (dp - drow[:, None])
+        dq[r0:r1] = scale * (ds @ k)
+        dk += scale * (ds.T @ q[r0:r1])
+        dvec[r0:r1] = drow
+    return dq, dk, dv, dvec
+
+
+def attention_bwd(q, k, v, do, scale: float, causal: bool, row_chunk: int = 512):
+    """dQ, dK, dV [B,H,N,d] and D [B,H,N] for fp64 inputs [B,H,N,d]."""
+    q = np.asarray(q, np.float64)
+    B, H, N, d = q.shape
+    dq = np.empty_like(q)
+    dk = np.empty_like(q)
+    dv = np.empty((B, H, N, np.asarray(v).shape[-1]))
+    dvec = np.empty((B, H, N))
+    for b in range(B):
+        for h in range(H):
+            dq[b, h], dk[b, h], dv[b, h], dvec[b, h] = attention_bwd_head(
+                q[b, h], k[b, h], v[b, h], do[b, h], scale, causal, row_chunk)
+    return dq, dk, dv, dvec
+
+
+def attention_bwd_rows(q_head, k_head, v_head, do_head, scale: float, causal: bool, rows):
+    """dQ rows and D for selected query rows of one head.
+
+    dQ_i = scale * sum_j P_ij (dP_ij - D_i) K_j needs only row i of P, so a sample of
+    rows is computed exactly from the definition without the full N x N matrices.
+    """
+    rows = np.asarray(rows, dtype=np.int64)
+    q = np.asarray(q_head, np.float64)
+    k = np.asarray(k_head, np.float64)
+    v = np.asarray(v_head, np.float64)
+    do = np.asarray(do_head, np.float64)[rows]
+    s = scores(q[rows], k, scale, causal, rows)
+    p, _, _ = _softmax_rows(s)
+    o = p @ v
+    dp = do @ v.T
+    drow = np.sum(do * o, axis=1)
+    ds = p * (dp - drow[:, None])
+    return scale * (ds @ k), drow
