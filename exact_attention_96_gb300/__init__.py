@@ -1,0 +1,9 @@
+"""Exact scaled-dot-product attention for GB300 (sm_103a).
+
+The compute path is libfa_gb300.so (hand-written TMA / tcgen05 / TMEM kernels behind the C
+ABI in include/fa.h).  This package only marshals arguments: ``abi`` mirrors the C entry
+points one to one, ``attention`` wraps them for torch tensors, ``inputs`` draws the seeded
+synthetic inputs, ``build`` compiles the library in-tree.
+"""
+
+from .attention import forward, backward, workspace_bytes, status_check  # noqa: F401

@@ -1,0 +1,93 @@
+"""ctypes view of the C ABI in include/fa.h (libfa_gb300.so).
+
+Argument marshalling only: every function here forwards to the same-named C entry point.
+Loading fails loudly when the library has not been built; there is no fallback path.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "lib", "libfa_gb300.so")
+
+FA_OK = 0
+FA_ERR_INVALID_ARG = 1
+FA_ERR_UNSUPPORTED = 2
+FA_ERR_MISALIGNED = 3
+FA_ERR_CUDA = 4
+FA_ERR_TIMEOUT = 5
+
+_c_void_p = ctypes.c_void_p
+_c_int = ctypes.c_int
+_c_float = ctypes.c_float
+_c_size_t = ctypes.c_size_t
+
+# name -> (restype, argtypes), in the order include/fa.h declares them
+SIGNATURES = {
+    "fa_fwd": (_c_int, [_c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_void_p,
+                        _c_int, _c_int, _c_int, _c_int, _c_float, _c_int, _c_void_p]),
+    "fa_bwd_workspace_bytes": (_c_size_t, [_c_int, _c_int, _c_int, _c_int]),
+    "fa_bwd": (_c_int, [_c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_void_p,
+                        _c_void_p, _c_void_p, _c_void_p,
+                        _c_int, _c_int, _c_int, _c_int, _c_float, _c_int,
+                        _c_void_p, _c_size_t, _c_void_p]),
+    "fa_status_check": (_c_int, [_c_void_p]),
+    "fa_status_string": (ctypes.c_char_p, [_c_int]),
+    "fa_set_wait_limit_ns": (ctypes.c_uint64, [ctypes.c_uint64]),
+}
+
+_lib = None
+
+
+class FAError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn} returned {status_string(status)} ({status})")
+
+
+def load(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Loads libfa_gb300.so (once) and declares every entry point's signature."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise FileNotFoundError(
+            f"{path} is missing: build it with `python -m exact_attention_96_gb300.build`")
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    return load().fa_status_string(status).decode()
+
+
+def check(fn: str, status: int) -> None:
+    if status != FA_OK:
+        raise FAError(fn, status)
+
+
+def fa_fwd(q, k, v, o, lse, B, H, N, d, scale, causal, stream) -> int:
+    return load().fa_fwd(q, k, v, o, lse, B, H, N, d, scale, int(causal), stream)
+
+
+def fa_bwd_workspace_bytes(B, H, N, d) -> int:
+    return load().fa_bwd_workspace_bytes(B, H, N, d)
+
+
+def fa_bwd(q, k, v, o, do, lse, dq, dk, dv, B, H, N, d, scale, causal, ws, ws_bytes, stream) -> int:
+    return load().fa_bwd(q, k, v, o, do, lse, dq, dk, dv, B, H, N, d, scale, int(causal),
+                         ws, ws_bytes, stream)
+
+
+def fa_status_check(stream) -> int:
+    return load().fa_status_check(stream)
+
+
+def fa_set_wait_limit_ns(ns: int) -> int:
+    return load().fa_set_wait_limit_ns(ns)

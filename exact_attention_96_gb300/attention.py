@@ -1,0 +1,73 @@
+"""PyTorch-facing calls: device memory and the current stream come from torch; all
+arithmetic runs in libfa_gb300.so (include/fa.h).  Tensors are bf16, contiguous,
+[B, H, N, d] on a CUDA device; LSE is fp32 [B, H, N].
+"""
+
+from __future__ import annotations
+
+import math
+
+import torch
+
+from . import abi
+
+
+def _check_qkv(*ts):
+    t0 = ts[0]
+    if t0.dim() != 4:
+        raise ValueError("expected [B, H, N, d] tensors")
+    for t in ts:
+        if not t.is_cuda or t.dtype != torch.bfloat16 or not t.is_contiguous():
+            raise ValueError("expected contiguous bf16 CUDA tensors")
+        if t.shape != t0.shape or t.device != t0.device:
+            raise ValueError("all tensors must share shape and device")
+
+
+def _stream(t: torch.Tensor) -> int:
+    return torch.cuda.current_stream(t.device).cuda_stream
+
+
+def forward(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None):
+    """O, LSE = attention(q, k, v); writes into `out` / `lse` when given."""
+    _check_qkv(q, k, v)
+    B, H, N, d = q.shape
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    o = torch.empty_like(q) if out is None else out
+    l = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if lse is None else lse
+    with torch.cuda.device(q.device):
+        st = abi.fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), l.data_ptr(),
+                        B, H, N, d, scale, causal, _stream(q))
+    abi.check("fa_fwd", st)
+    return o, l
+
+
+def workspace_bytes(B: int, H: int, N: int, d: int) -> int:
+    return abi.fa_bwd_workspace_bytes(B, H, N, d)
+
+
+def backward(q, k, v, o, do, lse, causal: bool = False, scale: float | None = None,
+             workspace=None, grads=None):
+    """dQ, dK, dV of attention for upstream gradient `do` (O and LSE from forward)."""
+    _check_qkv(q, k, v, o, do)
+    B, H, N, d = q.shape
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    nbytes = workspace_bytes(B, H, N, d)
+    if workspace is None:
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+    if grads is None:
+        grads = (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v))
+    dq, dk, dv = grads
+    with torch.cuda.device(q.device):
+        st = abi.fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(),
+                        lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+                        B, H, N, d, scale, causal, workspace.data_ptr(), workspace.numel(),
+                        _stream(q))
+    abi.check("fa_bwd", st)
+    return dq, dk, dv
+
+
+def status_check(device=None) -> int:
+    """Synchronises the current stream and returns the library's device status code."""
+    dev = torch.device("cuda") if device is None else torch.device(device)
+    with torch.cuda.device(dev):
+        return abi.fa_status_check(torch.cuda.current_stream(dev).cuda_stream)

@@ -1,0 +1,242 @@
+// fa_api.cu -- host side of the C ABI declared in include/fa.h: argument validation,
+// TMA tensor-map encoding, launches, and the per-device error word.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "../../include/fa.h"
+#include "fa_internal.h"
+
+namespace {
+
+// One error word per device, in static device memory.  Bit 0: a bounded wait timed out.
+// Bit 1: shared memory was not 1024-byte aligned.
+__device__ int g_fa_err_word;
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+int* g_err_ptr[kMaxDevices] = {};
+int g_cc_ok[kMaxDevices] = {};  // 0 unknown, 1 sm_103, -1 other
+std::atomic<uint64_t> g_wait_limit_ns{2000000000ull};
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+fa_status cuda_fail(cudaError_t) { return FA_ERR_CUDA; }
+
+// Resolves the device, checks it is compute capability 10.3 and returns its error word.
+fa_status device_setup(int* dev_out, int** err_out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return FA_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (g_cc_ok[dev] == 0) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+      return FA_ERR_CUDA;
+    g_cc_ok[dev] = (major == 10 && minor == 3) ? 1 : -1;
+  }
+  if (g_cc_ok[dev] != 1) return FA_ERR_UNSUPPORTED;
+  if (g_err_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_fa_err_word) != cudaSuccess) return FA_ERR_CUDA;
+    g_err_ptr[dev] = static_cast<int*>(p);
+  }
+  if (g_encode == nullptr) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || fn == nullptr)
+      return FA_ERR_CUDA;
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  *dev_out = dev;
+  *err_out = g_err_ptr[dev];
+  return FA_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+fa_status check_sizes(int B, int H, int N, int d) {
+  if (B < 1 || H < 1 || N < 1) return FA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128 && d != 256) return FA_ERR_UNSUPPORTED;
+  if ((long long)B * H > 65535 || N > (1 << 20)) return FA_ERR_UNSUPPORTED;
+  return FA_OK;
+}
+
+fa_status check_scale(float scale) {
+  if (!(scale > 0.f) || !std::isfinite(scale)) return FA_ERR_INVALID_ARG;
+  return FA_OK;
+}
+
+// [BH, N, d] bf16, box (64 columns, rows, 1), 128-byte swizzle.
+bool encode_bf16_rows(CUtensorMap* m, const void* p, int BH, int N, int d, int rows) {
+  const cuuint64_t dims[3] = {cuuint64_t(d), cuuint64_t(N), cuuint64_t(BH)};
+  const cuuint64_t strides[2] = {cuuint64_t(d) * 2, cuuint64_t(N) * d * 2};
+  const cuuint32_t box[3] = {64, cuuint32_t(rows), 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(p), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// [1, BH, Np] fp32 rows, box (128, 1, 1), no swizzle.
+bool encode_f32_rows(CUtensorMap* m, const void* p, int BH, int Np) {
+  const cuuint64_t dims[3] = {cuuint64_t(Np), cuuint64_t(BH), 1};
+  const cuuint64_t strides[2] = {cuuint64_t(Np) * 4, cuuint64_t(Np) * 4 * BH};
+  const cuuint32_t box[3] = {128, 1, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(p), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
+
+struct WsLayout {
+  size_t dvec_off, lse2_off, dq_off, total;
+  int Np, n_q_tiles;
+};
+
+WsLayout ws_layout(int B, int H, int N, int d) {
+  WsLayout w{};
+  const size_t BH = size_t(B) * H;
+  w.Np = (N + 3) & ~3;
+  w.n_q_tiles = (N + 127) / 128;
+  w.dvec_off = 0;
+  w.lse2_off = round256(BH * w.Np * 4);
+  w.dq_off = w.lse2_off + round256(BH * w.Np * 4);
+  w.total = w.dq_off + BH * size_t(w.n_q_tiles) * 128 * d * 4;
+  return w;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* fa_status_string(fa_status s) {
+  switch (s) {
+    case FA_OK: return "FA_OK";
+    case FA_ERR_INVALID_ARG: return "FA_ERR_INVALID_ARG";
+    case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED";
+    case FA_ERR_MISALIGNED: return "FA_ERR_MISALIGNED";
+    case FA_ERR_CUDA: return "FA_ERR_CUDA";
+    case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT";
+  }
+  return "FA_ERR_UNKNOWN";
+}
+
+uint64_t fa_set_wait_limit_ns(uint64_t ns) {
+  if (ns < 1000000ull) ns = 1000000ull;
+  return g_wait_limit_ns.exchange(ns);
+}
+
+fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
+                 int d, float scale, int causal, fa_stream_t stream) {
+  if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
+  fa_status st = check_sizes(B, H, N, d);
+  if (st != FA_OK) return st;
+  if ((st = check_scale(scale)) != FA_OK) return st;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+    return FA_ERR_MISALIGNED;
+  int dev = 0;
+  int* err = nullptr;
+  if ((st = device_setup(&dev, &err)) != FA_OK) return st;
+
+  const int BH = B * H;
+  fa::Maps maps;
+  const int kv_rows = fa::fwd_kv_tile(d);
+  if (!encode_bf16_rows(&maps.q, q, BH, N, d, 128) || !encode_bf16_rows(&maps.k, k, BH, N, d, kv_rows) ||
+      !encode_bf16_rows(&maps.v, v, BH, N, d, kv_rows) || !encode_bf16_rows(&maps.o, o, BH, N, d, 128))
+    return FA_ERR_CUDA;
+  fa::FwdArgs a;
+  a.lse = lse;
+  a.N = N;
+  a.BH = BH;
+  a.n_q_tiles = (N + 127) / 128;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.wait_limit_ns = g_wait_limit_ns.load();
+  a.err_word = err;
+  const cudaError_t e = fa::launch_fwd(maps, a, d, causal != 0, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : cuda_fail(e);
+}
+
+size_t fa_bwd_workspace_bytes(int B, int H, int N, int d) {
+  if (check_sizes(B, H, N, d) != FA_OK) return 0;
+  return ws_layout(B, H, N, d).total;
+}
+
+fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                 const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d, float scale,
+                 int causal, void* workspace, size_t workspace_bytes, fa_stream_t stream) {
+  if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv || !workspace) return FA_ERR_INVALID_ARG;
+  fa_status st = check_sizes(B, H, N, d);
+  if (st != FA_OK) return st;
+  if ((st = check_scale(scale)) != FA_OK) return st;
+  if (d == 256) return FA_ERR_UNSUPPORTED;
+  const WsLayout w = ws_layout(B, H, N, d);
+  if (workspace_bytes < w.total) return FA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dout) ||
+      !aligned16(lse) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv) ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return FA_ERR_MISALIGNED;
+  int dev = 0;
+  int* err = nullptr;
+  if ((st = device_setup(&dev, &err)) != FA_OK) return st;
+
+  const int BH = B * H;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  fa::BwdMaps maps;
+  CUtensorMap m_lse2, m_dvec, m_dk, m_dv;
+  if (!encode_bf16_rows(&maps.q, q, BH, N, d, 128) || !encode_bf16_rows(&maps.k, k, BH, N, d, 128) ||
+      !encode_bf16_rows(&maps.v, v, BH, N, d, 128) || !encode_bf16_rows(&maps.dout, dout, BH, N, d, 128) ||
+      !encode_bf16_rows(&m_dk, dk, BH, N, d, 128) || !encode_bf16_rows(&m_dv, dv, BH, N, d, 128) ||
+      !encode_f32_rows(&m_lse2, ws + w.lse2_off, BH, w.Np) || !encode_f32_rows(&m_dvec, ws + w.dvec_off, BH, w.Np))
+    return FA_ERR_CUDA;
+  fa::BwdArgs a;
+  a.q = static_cast<const uint16_t*>(q);
+  a.k = static_cast<const uint16_t*>(k);
+  a.v = static_cast<const uint16_t*>(v);
+  a.o = static_cast<const uint16_t*>(o);
+  a.dout = static_cast<const uint16_t*>(dout);
+  a.lse = lse;
+  a.dq = static_cast<uint16_t*>(dq);
+  a.dk = static_cast<uint16_t*>(dk);
+  a.dv = static_cast<uint16_t*>(dv);
+  a.dvec = reinterpret_cast<float*>(ws + w.dvec_off);
+  a.dq_acc = reinterpret_cast<float*>(ws + w.dq_off);
+  a.N = N;
+  a.BH = BH;
+  a.d = d;
+  a.scale = scale;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.wait_limit_ns = g_wait_limit_ns.load();
+  a.err_word = err;
+  const cudaError_t e = fa::launch_bwd_all(maps, m_lse2, m_dvec, m_dk, m_dv, a, causal != 0, w.Np,
+                                           reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : cuda_fail(e);
+}
+
+fa_status fa_status_check(fa_stream_t stream) {
+  int dev = 0;
+  int* err = nullptr;
+  fa_status st = device_setup(&dev, &err);
+  if (st != FA_OK) return st;
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return FA_ERR_CUDA;
+  int word = 0;
+  if (cudaMemcpyFromSymbol(&word, g_fa_err_word, sizeof(int)) != cudaSuccess) return FA_ERR_CUDA;
+  if (word != 0) {
+    const int zero = 0;
+    if (cudaMemcpyToSymbol(g_fa_err_word, &zero, sizeof(int)) != cudaSuccess) return FA_ERR_CUDA;
+  }
+  if (word & 1) return FA_ERR_TIMEOUT;
+  if (word != 0) return FA_ERR_CUDA;
+  return FA_OK;
+}
+
+}  // extern "C"

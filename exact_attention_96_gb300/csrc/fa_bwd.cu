@@ -1,0 +1,548 @@
+// fa_bwd.cu -- backward pass of exact attention on sm_103a.
+//
+// Only O and the per-row log-sum-exp were kept by the forward pass; S and P are recomputed
+// block by block from Q, K, V ("FlashAttention 与显存" §09).  The gradients are those of
+// O = softmax(scale * Q K^T) V:
+//   dV = P^T dO,  dP = dO V^T,  D_i = rowsum(dO_i * O_i),  dS = P * (dP - D),
+//   dQ = scale * dS K,  dK = scale * dS^T Q.
+//
+// Three launches on one stream:
+//   1. fa_bwd_prep_kernel   D = rowsum(dO * O), LSE2 = LSE * log2(e) (both fp32, rows padded
+//                           to a multiple of 4), and a zeroed fp32 dQ accumulator.
+//   2. fa_bwd_main_kernel   one CTA per tile of 128 keys of one (batch, head); it keeps K_j,
+//                           V_j and the dK_j, dV_j accumulators on chip and loops over the
+//                           query tiles, adding each tile's dQ contribution into the fp32
+//                           accumulator in global memory (no second pass over S).
+//   3. fa_bwd_dq_kernel     dQ accumulator * scale -> bf16 dQ.
+//
+// fa_bwd_main_kernel roles (thread t of a warpgroup owns TMEM lane t):
+//   warps 0-3  key rows: P^T = 2^(S^T*scale*log2e - LSE2) (masked) -> bf16 into TMEM for
+//              the dV product; dS^T = P^T (dP^T - D) -> bf16 into shared memory for the dK
+//              and dQ products; finally dK, dV -> bf16 -> TMA stores.
+//   warps 4-7  query rows: read each finished dQ tile from TMEM and add it (fp32 vector
+//              atomics, coalesced by the accumulator's tile layout) into global memory.
+//   warp 8     TMA producer: K_j, V_j once; then Q_i, dO_i, LSE2_i, D_i through a ring.
+//   warp 9     TMEM allocator and MMA issuer:
+//                S^T  = K_j Q_i^T        (SS)  -> TMEM [0,128)
+//                dP^T = V_j dO_i^T       (SS)  -> TMEM [128,256)
+//                dV  += P^T dO_i         (TS, P^T from TMEM [0,64))
+//                dK  += dS^T Q_i         (SS, dS^T K-major in smem)
+//                dQ_i = dS K_j           (SS, the same dS^T buffer read M-major) -> TMEM [128,..)
+//   The dQ tile reuses the dP^T columns (dP^T is fully read before dS is published), and the
+//   next S^T overwrites P^T only after the dV product that reads it has completed.
+//
+// dQ accumulator layout (fp32): [B*H][q tile][d/4][128 rows][4] -- for a fixed group of four
+// columns, the 128 rows of a tile are contiguous, so the 32 lanes of a warp adding one
+// float4 each touch one contiguous 512-byte span.
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "fa_internal.h"
+#include "sm103_ptx.cuh"
+
+namespace fa {
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+// ----------------------------------------------------------------- prep ----
+
+template <int D>
+__global__ void __launch_bounds__(256)
+fa_bwd_prep_kernel(const uint16_t* __restrict__ o, const uint16_t* __restrict__ dout,
+                   const float* __restrict__ lse, float* __restrict__ dvec,
+                   float* __restrict__ lse2, float* __restrict__ dq_acc, int N, int Np,
+                   int n_q_tiles, int BH) {
+  constexpr int kTPR = D / 8;              // threads per row, 8 elements each
+  constexpr int kRowsPerBlock = 256 / kTPR;
+  const int sub = threadIdx.x % kTPR;
+  const long long prow = (long long)blockIdx.x * kRowsPerBlock + threadIdx.x / kTPR;  // padded row id
+  const long long rows_padded = (long long)BH * n_q_tiles * 128;
+  if (prow >= rows_padded) return;
+  const int bh = int(prow / (n_q_tiles * 128));
+  const int i = int(prow % (n_q_tiles * 128));
+
+  // zero this row's part of the dQ accumulator tile: column groups 2*sub, 2*sub+1
+  {
+    const int qt = i >> 7, t = i & 127;
+    float4* tile = reinterpret_cast<float4*>(dq_acc + ((size_t)bh * n_q_tiles + qt) * 128 * D);
+    tile[(2 * sub) * 128 + t] = make_float4(0.f, 0.f, 0.f, 0.f);
+    tile[(2 * sub + 1) * 128 + t] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  float acc = 0.f;
+  if (i < N) {
+    const size_t off = ((size_t)bh * N + i) * D + sub * 8;
+    const uint4 a = *reinterpret_cast<const uint4*>(o + off);
+    const uint4 b = *reinterpret_cast<const uint4*>(dout + off);
+    const uint32_t av[4] = {a.x, a.y, a.z, a.w};
+    const uint32_t bv[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      acc = fmaf(__uint_as_float(av[e] << 16), __uint_as_float(bv[e] << 16), acc);
+      acc = fmaf(__uint_as_float(av[e] & 0xFFFF0000u), __uint_as_float(bv[e] & 0xFFFF0000u), acc);
+    }
+  }
+#pragma unroll
+  for (int w = kTPR / 2; w >= 1; w >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, w);
+  if (sub == 0 && i < Np) {
+    dvec[(size_t)bh * Np + i] = (i < N) ? acc : 0.f;
+    lse2[(size_t)bh * Np + i] = (i < N) ? lse[(size_t)bh * N + i] * kLog2e : 0.f;
+  }
+}
+
+// ------------------------------------------------------------ dq convert ----
+
+template <int D>
+__global__ void __launch_bounds__(256)
+fa_bwd_dq_kernel(const float* __restrict__ dq_acc, uint16_t* __restrict__ dq, int N, int n_q_tiles,
+                 int BH, float scale) {
+  // thread -> (tile row t = fastest, group of 8 columns k)
+  constexpr int kK = D / 8;
+  const long long gid = (long long)blockIdx.x * 256 + threadIdx.x;
+  const long long per_tile = 128LL * kK;
+  const long long total = (long long)BH * n_q_tiles * per_tile;
+  if (gid >= total) return;
+  const long long tile = gid / per_tile;
+  const int rem = int(gid % per_tile);
+  const int t = rem & 127, k = rem >> 7;
+  const int bh = int(tile / n_q_tiles), qt = int(tile % n_q_tiles);
+  const int i = qt * 128 + t;
+  if (i >= N) return;
+  const float4* src = reinterpret_cast<const float4*>(dq_acc + (size_t)tile * 128 * D);
+  const float4 a = src[(2 * k) * 128 + t];
+  const float4 b = src[(2 * k + 1) * 128 + t];
+  uint4 w;
+  w.x = pack_bf16x2(a.x * scale, a.y * scale);
+  w.y = pack_bf16x2(a.z * scale, a.w * scale);
+  w.z = pack_bf16x2(b.x * scale, b.y * scale);
+  w.w = pack_bf16x2(b.z * scale, b.w * scale);
+  *reinterpret_cast<uint4*>(dq + ((size_t)bh * N + i) * D + k * 8) = w;
+}
+
+// ------------------------------------------------------------------ main ----
+
+constexpr int kTile = 128;  // keys per CTA and queries per inner step
+constexpr int kMainThreads = 320;
+
+template <int D, int NS>
+struct BwdLayout {
+  static constexpr int kSlabs = D / 64;
+  static constexpr int kTileBytes = kTile * D * 2;   // one [128 x D] bf16 tile
+  static constexpr int kKOff = 0;
+  static constexpr int kVOff = kKOff + kTileBytes;
+  static constexpr int kQOff = kVOff + kTileBytes;            // NS stages
+  static constexpr int kdOOff = kQOff + NS * kTileBytes;      // NS stages
+  static constexpr int kdSOff = kdOOff + NS * kTileBytes;     // [128 keys x 128 queries] bf16
+  static constexpr int kdSBytes = kTile * kTile * 2;
+  static constexpr int kLseOff = kdSOff + kdSBytes;           // NS x 128 fp32
+  static constexpr int kDOff = kLseOff + NS * 512;            // NS x 128 fp32
+  static constexpr int kBarOff = kDOff + NS * 512;
+  static constexpr int kBarKV = 0;
+  static constexpr int kBarQFull = 1;
+  static constexpr int kBarQEmpty = kBarQFull + NS;
+  static constexpr int kBarSFull = kBarQEmpty + NS;
+  static constexpr int kBarDPFull = kBarSFull + 1;
+  static constexpr int kBarPReady = kBarDPFull + 1;
+  static constexpr int kBarDSReady = kBarPReady + 1;
+  static constexpr int kBarDVDone = kBarDSReady + 1;
+  static constexpr int kBarDQFull = kBarDVDone + 1;
+  static constexpr int kBarDQDrained = kBarDQFull + 1;
+  static constexpr int kBarDSFree = kBarDQDrained + 1;
+  static constexpr int kBarAccDone = kBarDSFree + 1;
+  static constexpr int kBarEpi = kBarAccDone + 1;
+  static constexpr int kBarDrain = kBarEpi + 1;
+  static constexpr int kNumBars = kBarDrain + 1;
+  static constexpr int kMiscOff = kBarOff + kNumBars * 8;
+  static constexpr int kBytes = kMiscOff + 16;
+  // TMEM columns
+  static constexpr int kColS = 0;
+  static constexpr int kColDP = 128;   // dP^T, then the dQ tile
+  static constexpr int kColDV = 256;
+  static constexpr int kColDK = 256 + D;
+  static constexpr int kTmemCols = 512;
+  static constexpr uint32_t kStageTx = 2 * kTileBytes + 2 * 512;
+  static_assert(256 + 2 * D <= 512, "TMEM budget");
+  static_assert(kBytes <= 232448, "shared memory budget");
+};
+
+template <int D, int NS, bool CAUSAL>
+__global__ void __launch_bounds__(kMainThreads, 1)
+fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
+                   const __grid_constant__ CUtensorMap tmLse2, const __grid_constant__ CUtensorMap tmD,
+                   const __grid_constant__ CUtensorMap tmdK, const __grid_constant__ CUtensorMap tmdV,
+                   const BwdArgs args) {
+  using L = BwdLayout<D, NS>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t base = smem_addr(smem_raw);
+  if (base & 1023u) {  // the 128-byte swizzle needs 1024-byte aligned tiles
+    if (threadIdx.x == 0) atomicOr(args.err_word, 2);
+    return;
+  }
+  uint8_t* smem = smem_raw;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int bh = blockIdx.y;
+  const int kv_tile = blockIdx.x;
+  const int k0 = kv_tile * kTile;
+  const int N = args.N;
+  const int n_q_tiles = (N + kTile - 1) / kTile;
+  const int it_first = CAUSAL ? kv_tile : 0;  // query tiles before the diagonal see none of these keys
+  const int n_it = n_q_tiles - it_first;
+
+  auto bar = [&](int i) -> uint32_t { return base + L::kBarOff + 8u * uint32_t(i); };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMiscOff + 4);
+  const WaitCtl wc{abort_flag, args.err_word, args.wait_limit_ns};
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(L::kBarKV), 1);
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(bar(L::kBarQFull + s), 1);
+      mbar_init(bar(L::kBarQEmpty + s), 128 + 1);  // key-row warps + MMA commit
+    }
+    mbar_init(bar(L::kBarSFull), 1);
+    mbar_init(bar(L::kBarDPFull), 1);
+    mbar_init(bar(L::kBarPReady), 128);
+    mbar_init(bar(L::kBarDSReady), 128);
+    mbar_init(bar(L::kBarDVDone), 1);
+    mbar_init(bar(L::kBarDQFull), 1);
+    mbar_init(bar(L::kBarDQDrained), 128);
+    mbar_init(bar(L::kBarDSFree), 1);
+    mbar_init(bar(L::kBarAccDone), 1);
+    mbar_init(bar(L::kBarEpi), 128);
+    mbar_init(bar(L::kBarDrain), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 9) {
+    tmem_alloc(smem_addr(tmem_slot), L::kTmemCols);
+    tmem_relinquish_alloc_permit();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+
+  const uint32_t sK = base + L::kKOff, sV = base + L::kVOff, sdS = base + L::kdSOff;
+  auto sQ = [&](int s) -> uint32_t { return base + L::kQOff + uint32_t(s) * L::kTileBytes; };
+  auto sdO = [&](int s) -> uint32_t { return base + L::kdOOff + uint32_t(s) * L::kTileBytes; };
+
+  if (warp == 8) {
+    // ------------------------------------------------------------ producer ----
+    if (lane == 0) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      tma_prefetch_desc(&tmdO);
+      mbar_arrive_expect_tx(bar(L::kBarKV), 2 * L::kTileBytes);
+      for (int s = 0; s < L::kSlabs; ++s) {
+        tma_load_3d(sK + s * (kTile * 128), &tmK, bar(L::kBarKV), s * 64, k0, bh);
+        tma_load_3d(sV + s * (kTile * 128), &tmV, bar(L::kBarKV), s * 64, k0, bh);
+      }
+      int arms[NS];
+#pragma unroll
+      for (int s = 0; s < NS; ++s) arms[s] = 0;
+      bool ok = true;
+      for (int it = 0; it < n_it; ++it) {
+        const int st = it % NS;
+        if (it >= NS && !mbar_wait(bar(L::kBarQEmpty + st), ((it / NS) - 1) & 1, wc)) { ok = false; break; }
+        const int q0 = (it_first + it) * kTile;
+        const uint32_t fb = bar(L::kBarQFull + st);
+        mbar_arrive_expect_tx(fb, L::kStageTx);
+        for (int s = 0; s < L::kSlabs; ++s) {
+          tma_load_3d(sQ(st) + s * (kTile * 128), &tmQ, fb, s * 64, q0, bh);
+          tma_load_3d(sdO(st) + s * (kTile * 128), &tmdO, fb, s * 64, q0, bh);
+        }
+        tma_load_3d(base + L::kLseOff + st * 512, &tmLse2, fb, q0, bh, 0);
+        tma_load_3d(base + L::kDOff + st * 512, &tmD, fb, q0, bh, 0);
+        ++arms[st];
+      }
+      if (!ok) {
+        auto drain = [&](uint32_t b, uint32_t parity) {
+          for (uint64_t t0 = global_timer_ns();
+               !mbar_try_wait(b, parity) && global_timer_ns() - t0 < wc.limit_ns;) {
+          }
+        };
+        drain(bar(L::kBarKV), 0);
+        for (int s = 0; s < NS; ++s)
+          if (arms[s] > 0) drain(bar(L::kBarQFull + s), (arms[s] - 1) & 1);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 9) {
+    // ---------------------------------------------------------- MMA issuer ----
+    if (lane == 0) {
+      constexpr uint32_t kIdSq = idesc_bf16_f32(128, 128, 0, 0);  // S^T, dP^T
+      constexpr uint32_t kIdAcc = idesc_bf16_f32(128, D, 0, 1);   // dV, dK: B N-major
+      constexpr uint32_t kIdDQ = idesc_bf16_f32(128, D, 1, 1);    // dQ: A (dS) M-major, B N-major
+      bool ok = mbar_wait(bar(L::kBarKV), 0, wc);
+      for (int it = 0; ok && it < n_it; ++it) {
+        const int st = it % NS;
+        const uint32_t ph = it & 1;
+        if (!mbar_wait(bar(L::kBarQFull + st), (it / NS) & 1, wc)) { ok = false; break; }
+        if (it > 0 && !mbar_wait(bar(L::kBarDVDone), ph ^ 1, wc)) { ok = false; break; }
+        tc_fence_after_sync();
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * (kTile * 128) + (kk & 3) * 32;
+          mma_ss(tmem + L::kColS, sdesc_sw128(sK + off, 16, 1024), sdesc_sw128(sQ(st) + off, 16, 1024),
+                 kIdSq, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(bar(L::kBarSFull));
+        if (it > 0 && !mbar_wait(bar(L::kBarDQDrained), ph ^ 1, wc)) { ok = false; break; }
+        tc_fence_after_sync();
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * (kTile * 128) + (kk & 3) * 32;
+          mma_ss(tmem + L::kColDP, sdesc_sw128(sV + off, 16, 1024), sdesc_sw128(sdO(st) + off, 16, 1024),
+                 kIdSq, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(bar(L::kBarDPFull));
+        if (!mbar_wait(bar(L::kBarPReady), ph, wc)) { ok = false; break; }
+        tc_fence_after_sync();
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk) {
+          mma_ts(tmem + L::kColDV, tmem + L::kColS + kk * 8,
+                 sdesc_sw128(sdO(st) + kk * (16 * 128), kTile * 128, 1024), kIdAcc,
+                 (it > 0 || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(bar(L::kBarDVDone));
+        if (!mbar_wait(bar(L::kBarDSReady), ph, wc)) { ok = false; break; }
+        tc_fence_after_sync();
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk) {
+          const uint32_t a_off = (kk >> 2) * (kTile * 128) + (kk & 3) * 32;  // dS^T K-major
+          mma_ss(tmem + L::kColDK, sdesc_sw128(sdS + a_off, 16, 1024),
+                 sdesc_sw128(sQ(st) + kk * (16 * 128), kTile * 128, 1024), kIdAcc,
+                 (it > 0 || kk > 0) ? 1u : 0u);
+        }
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk) {
+          mma_ss(tmem + L::kColDP, sdesc_sw128(sdS + kk * (16 * 128), kTile * 128, 1024),
+                 sdesc_sw128(sK + kk * (16 * 128), kTile * 128, 1024), kIdDQ, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(bar(L::kBarDQFull));
+        mma_commit(bar(L::kBarDSFree));
+        mma_commit(bar(L::kBarQEmpty + st));
+      }
+      if (ok) mma_commit(bar(L::kBarAccDone));
+      mma_commit(bar(L::kBarDrain));
+      for (uint64_t t0 = global_timer_ns();
+           !mbar_try_wait(bar(L::kBarDrain), 0) && global_timer_ns() - t0 < wc.limit_ns;) {
+      }
+    }
+    __syncwarp();
+  } else if (warp < 4) {
+    // ------------------------------------------------------------ key rows ----
+    const int t = threadIdx.x;  // key row within the tile = TMEM lane
+    const uint32_t lane_off = uint32_t(warp * 32) << 16;
+    const int key = k0 + t;
+    const float sl2 = args.scale_log2;
+    bool ok = true;
+    for (int it = 0; it < n_it; ++it) {
+      const int st = it % NS;
+      const uint32_t ph = it & 1;
+      const int q0 = (it_first + it) * kTile;
+      const bool edge = (CAUSAL && it == 0) || (q0 + kTile > N);  // any masking in this tile
+      const float* lse2 = reinterpret_cast<const float*>(smem + L::kLseOff + st * 512);
+      const float* dv = reinterpret_cast<const float*>(smem + L::kDOff + st * 512);
+      // phase 1: P^T
+      if (!__all_sync(0xffffffffu, mbar_wait(bar(L::kBarSFull), ph, wc))) { ok = false; break; }
+      tc_fence_after_sync();
+#pragma unroll 1
+      for (int c = 0; c < kTile; c += 32) {
+        uint32_t r[32];
+        tmem_ld32(tmem + lane_off + L::kColS + c, r);
+        uint32_t w[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          float p0 = ex2_approx(fmaf(__uint_as_float(r[e]), sl2, -lse2[c + e]));
+          float p1 = ex2_approx(fmaf(__uint_as_float(r[e + 1]), sl2, -lse2[c + e + 1]));
+          if (edge) {
+            const int qa = q0 + c + e;
+            if (qa >= N || (CAUSAL && qa < key)) p0 = 0.f;
+            if (qa + 1 >= N || (CAUSAL && qa + 1 < key)) p1 = 0.f;
+          }
+          w[e / 2] = pack_bf16x2(p0, p1);
+        }
+        tmem_st16(tmem + lane_off + L::kColS + c / 2, w);
+      }
+      tmem_wait_st();
+      tc_fence_before_sync();
+      mbar_arrive(bar(L::kBarPReady));
+      // phase 2: dS^T = P^T (dP^T - D)
+      bool got = mbar_wait(bar(L::kBarDPFull), ph, wc);
+      if (it > 0) got = got && mbar_wait(bar(L::kBarDSFree), ph ^ 1, wc);
+      if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
+      tc_fence_after_sync();
+#pragma unroll 1
+      for (int c = 0; c < kTile; c += 32) {
+        uint32_t r[32];
+        uint32_t pr[16];
+        tmem_ld32(tmem + lane_off + L::kColDP + c, r);
+        tmem_ld16(tmem + lane_off + L::kColS + c / 2, pr);
+        uint32_t w[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          const float p0 = __uint_as_float(pr[e / 2] << 16);
+          const float p1 = __uint_as_float(pr[e / 2] & 0xFFFF0000u);
+          float ds0 = p0 * (__uint_as_float(r[e]) - dv[c + e]);
+          float ds1 = p1 * (__uint_as_float(r[e + 1]) - dv[c + e + 1]);
+          if (edge) {
+            const int qa = q0 + c + e;
+            if (qa >= N) ds0 = 0.f;
+            if (qa + 1 >= N) ds1 = 0.f;
+          }
+          w[e / 2] = pack_bf16x2(ds0, ds1);
+        }
+        // dS^T row t, queries c..c+31 -> 128-byte swizzled [2 slabs x 128 rows x 128 B]
+        const int slab = c >> 6;
+        const int chunk0 = (c & 63) >> 3;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int phys = (chunk0 + i) ^ (t & 7);
+          *reinterpret_cast<uint4*>(smem + L::kdSOff + slab * (kTile * 128) + t * 128 + phys * 16) =
+              make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before_sync();
+      mbar_arrive(bar(L::kBarDSReady));
+      mbar_arrive(bar(L::kBarQEmpty + st));
+    }
+    // epilogue: dV then dK (scaled), staged in shared memory, TMA-stored
+    bool fin = ok && __all_sync(0xffffffffu, mbar_wait(bar(L::kBarAccDone), 0, wc));
+    if (fin) {
+      tc_fence_after_sync();
+      for (int which = 0; which < 2; ++which) {
+        const uint32_t col = which == 0 ? L::kColDV : L::kColDK;
+        const float mul = which == 0 ? 1.f : args.scale;
+        uint8_t* stage = smem + (which == 0 ? L::kQOff : L::kdOOff);  // stage 0 buffers, free now
+#pragma unroll 1
+        for (int c = 0; c < D; c += 32) {
+          uint32_t r[32];
+          tmem_ld32(tmem + lane_off + col + c, r);
+          uint32_t w[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            w[e] = pack_bf16x2(__uint_as_float(r[2 * e]) * mul, __uint_as_float(r[2 * e + 1]) * mul);
+          const int slab = c >> 6;
+          const int chunk0 = (c & 63) >> 3;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int phys = (chunk0 + i) ^ (t & 7);
+            *reinterpret_cast<uint4*>(stage + slab * (kTile * 128) + t * 128 + phys * 16) =
+                make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+          }
+        }
+      }
+      fence_proxy_async_smem();
+    }
+    mbar_arrive(bar(L::kBarEpi));
+    if (t == 0 && fin) {
+      if (mbar_wait(bar(L::kBarEpi), 0, wc) && *abort_flag == 0) {
+        for (int s = 0; s < L::kSlabs; ++s) {
+          tma_store_3d(&tmdV, sQ(0) + s * (kTile * 128), s * 64, k0, bh);
+          tma_store_3d(&tmdK, sdO(0) + s * (kTile * 128), s * 64, k0, bh);
+        }
+        bulk_commit_group();
+        bulk_wait_group_all();
+      }
+    }
+  } else {
+    // --------------------------------------------------------- query rows ----
+    const int t = threadIdx.x - 128;
+    const uint32_t lane_off = uint32_t((warp - 4) * 32) << 16;
+    const int n_tiles_total = n_q_tiles;
+    for (int it = 0; it < n_it; ++it) {
+      const int qt = it_first + it;
+      if (!__all_sync(0xffffffffu, mbar_wait(bar(L::kBarDQFull), it & 1, wc))) break;
+      tc_fence_after_sync();
+      float4* dst = reinterpret_cast<float4*>(args.dq_acc + ((size_t)bh * n_tiles_total + qt) * 128 * D);
+      uint32_t r[D];
+#pragma unroll
+      for (int c = 0; c < D; c += 32) {
+        uint32_t chunk[32];
+        tmem_ld32(tmem + lane_off + L::kColDP + c, chunk);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) r[c + e] = chunk[e];
+      }
+      // the whole dQ row is in registers: hand the TMEM columns back to the MMA warp
+      tc_fence_before_sync();
+      mbar_arrive(bar(L::kBarDQDrained));
+      if (qt * kTile + t < N) {
+#pragma unroll
+        for (int g = 0; g < D / 4; ++g)
+          atomicAdd(dst + g * 128 + t,
+                    make_float4(__uint_as_float(r[4 * g]), __uint_as_float(r[4 * g + 1]),
+                                __uint_as_float(r[4 * g + 2]), __uint_as_float(r[4 * g + 3])));
+      }
+    }
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, L::kTmemCols);
+  }
+}
+
+template <int D, int NS, bool CAUSAL>
+cudaError_t launch_main(const BwdMaps& m, const CUtensorMap& lse2, const CUtensorMap& dmap,
+                        const CUtensorMap& dk, const CUtensorMap& dv, const BwdArgs& a, cudaStream_t s) {
+  using L = BwdLayout<D, NS>;
+  auto kern = fa_bwd_main_kernel<D, NS, CAUSAL>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
+  if (e != cudaSuccess) return e;
+  dim3 grid((a.N + kTile - 1) / kTile, a.BH);
+  kern<<<grid, kMainThreads, L::kBytes, s>>>(m.q, m.k, m.v, m.dout, lse2, dmap, dk, dv, a);
+  return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_prep_and_convert(const BwdArgs& a, int Np, int n_q_tiles, cudaStream_t s, bool prep) {
+  if (prep) {
+    constexpr int kRowsPerBlock = 256 / (D / 8);
+    const long long rows = (long long)a.BH * n_q_tiles * 128;
+    const unsigned grid = unsigned((rows + kRowsPerBlock - 1) / kRowsPerBlock);
+    fa_bwd_prep_kernel<D><<<grid, 256, 0, s>>>(a.o, a.dout, a.lse, a.dvec, a.dvec + (size_t)a.BH * Np,
+                                               a.dq_acc, a.N, Np, n_q_tiles, a.BH);
+  } else {
+    const long long total = (long long)a.BH * n_q_tiles * 128 * (D / 8);
+    const unsigned grid = unsigned((total + 255) / 256);
+    fa_bwd_dq_kernel<D><<<grid, 256, 0, s>>>(a.dq_acc, a.dq, a.N, n_q_tiles, a.BH, a.scale);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+// Workspace: [D: BH x Np][LSE2: BH x Np][dQ accumulator: BH x n_q_tiles x 128 x d], fp32.
+cudaError_t launch_bwd_all(const BwdMaps& m, const CUtensorMap& lse2, const CUtensorMap& dmap,
+                           const CUtensorMap& dk, const CUtensorMap& dv, const BwdArgs& a, bool causal,
+                           int Np, cudaStream_t s) {
+  const int n_q_tiles = (a.N + kTile - 1) / kTile;
+  cudaError_t e;
+  switch (a.d) {
+    case 64:
+      if ((e = launch_prep_and_convert<64>(a, Np, n_q_tiles, s, true)) != cudaSuccess) return e;
+      e = causal ? launch_main<64, 3, true>(m, lse2, dmap, dk, dv, a, s)
+                 : launch_main<64, 3, false>(m, lse2, dmap, dk, dv, a, s);
+      if (e != cudaSuccess) return e;
+      return launch_prep_and_convert<64>(a, Np, n_q_tiles, s, false);
+    case 128:
+      if ((e = launch_prep_and_convert<128>(a, Np, n_q_tiles, s, true)) != cudaSuccess) return e;
+      e = causal ? launch_main<128, 2, true>(m, lse2, dmap, dk, dv, a, s)
+                 : launch_main<128, 2, false>(m, lse2, dmap, dk, dv, a, s);
+      if (e != cudaSuccess) return e;
+      return launch_prep_and_convert<128>(a, Np, n_q_tiles, s, false);
+    default:
+      return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace fa

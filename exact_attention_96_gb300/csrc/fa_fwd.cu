@@ -1,0 +1,391 @@
+// fa_fwd.cu -- forward pass of exact attention on sm_103a.
+//
+// One CTA owns one tile of 128 query rows of one (batch, head) and streams every key /
+// value tile of that head past it ("FlashAttention 与显存" §07: the second-version order,
+// one Q block per SM with K and V flying in; "FlashAttention算子优化" §2), keeping the
+// running maximum m and running sum l of each row and rescaling the output accumulator
+// when the maximum grows ("FlashAttention 与显存" §08).  S and P never leave the SM.
+//
+// Roles (warp specialisation, as the third version does with producer / consumer
+// warps, "FlashAttention 与显存" §11 -- re-derived here for TMA + tcgen05 + TMEM):
+//   warps 0-3  softmax: thread t owns query row t (= TMEM lane t).  Reads S from TMEM,
+//              masks, updates (m, l), writes P (bf16) back to TMEM, rescales O in TMEM
+//              when its warp's maximum grew, and finally normalises O, stages it in
+//              shared memory for a TMA store and writes LSE.
+//   warp 4     TMA producer: Q once, then K_j and V_j through an NS-stage ring.
+//   warp 5     TMEM allocator and MMA issuer (one thread):
+//                S_j = Q K_j^T        (tcgen05.mma, A and B from shared memory)
+//                O  += P_j V_j        (tcgen05.mma, A = P from TMEM, B = V from smem)
+//              S is double-buffered so S_{j+1} is computed while row softmax of S_j runs.
+//
+// TMEM columns (fp32 32-bit cells, 128 lanes): S0 [0, BC), S1 [BC, 2BC),
+// P0 / P1 bf16 pairs [2BC, 2BC + BC/2) and [2BC + BC/2, 3BC), O [3BC, 3BC + D).
+//
+// Shared memory, 1024-byte aligned (128-byte swizzle atoms): Q [D/64 slabs x 128 rows x
+// 128 B], K ring, V ring (each [D/64 slabs x BC rows x 128 B] per stage), barriers.
+// The Q region is reused to stage the bf16 output tile for the TMA store.
+//
+// Every wait is bounded (see WaitCtl): on timeout the kernel records the error, skips the
+// rest of the work, waits for its own copies and MMAs to land and frees TMEM.
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "fa_internal.h"
+#include "sm103_ptx.cuh"
+
+namespace fa {
+namespace {
+
+constexpr int kBM = 128;            // query rows per CTA (= TMEM lanes)
+constexpr int kSoftmaxThreads = 128;
+constexpr int kThreads = 192;       // 4 softmax warps + producer warp + MMA warp
+
+template <int D, int BC, int NS>
+struct FwdLayout {
+  static constexpr int kSlabs = D / 64;
+  static constexpr int kQBytes = kBM * D * 2;
+  static constexpr int kKVBytes = BC * D * 2;
+  static constexpr int kQOff = 0;
+  static constexpr int kKOff = kQBytes;
+  static constexpr int kVOff = kKOff + NS * kKVBytes;
+  static constexpr int kBarOff = kVOff + NS * kKVBytes;
+  // barrier slots
+  static constexpr int kBarQFull = 0;
+  static constexpr int kBarKFull = 1;
+  static constexpr int kBarKEmpty = kBarKFull + NS;
+  static constexpr int kBarVFull = kBarKEmpty + NS;
+  static constexpr int kBarVEmpty = kBarVFull + NS;
+  static constexpr int kBarSFull = kBarVEmpty + NS;  // 2
+  static constexpr int kBarSFree = kBarSFull + 2;    // 2
+  static constexpr int kBarPFull = kBarSFree + 2;    // 2
+  static constexpr int kBarODone = kBarPFull + 2;
+  static constexpr int kBarDrain = kBarODone + 1;
+  static constexpr int kBarEpi = kBarDrain + 1;
+  static constexpr int kNumBars = kBarEpi + 1;
+  static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // tmem slot, abort flag
+  static constexpr int kBytes = kMiscOff + 16;
+  static constexpr int kSmemAlloc = kBytes + 1024;  // slack for the 1024-byte alignment
+  // TMEM columns
+  static constexpr int kColS = 0;
+  static constexpr int kColP = 2 * BC;
+  static constexpr int kColO = 3 * BC;
+  static constexpr int kTmemUsed = 3 * BC + D;
+  static constexpr int kTmemCols = kTmemUsed <= 256 ? 256 : 512;
+  static_assert(kTmemUsed <= 512, "TMEM budget");
+  static_assert(kSmemAlloc <= 232448, "shared memory budget");
+  static_assert(D % 64 == 0 && BC % 32 == 0 && BC <= 256, "tile shape");
+};
+
+template <int D, int BC, int NS, bool CAUSAL>
+__global__ void __launch_bounds__(kThreads, 1)
+fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+              const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+              const FwdArgs args) {
+  using L = FwdLayout<D, BC, NS>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_addr(smem_raw);
+  const uint32_t base = (raw_addr + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (base - raw_addr);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int bh = blockIdx.y;
+  const int q_tile = CAUSAL ? (args.n_q_tiles - 1 - int(blockIdx.x)) : int(blockIdx.x);
+  const int q0 = q_tile * kBM;
+  const int N = args.N;
+  const int n_kv_all = (N + BC - 1) / BC;
+  const int nkv = CAUSAL ? min(n_kv_all, (q0 + kBM + BC - 1) / BC) : n_kv_all;
+
+  auto bar = [&](int i) -> uint32_t { return base + L::kBarOff + 8u * uint32_t(i); };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMiscOff + 4);
+  const WaitCtl wc{abort_flag, args.err_word, args.wait_limit_ns};
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(L::kBarQFull), 1);
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(bar(L::kBarKFull + s), 1);
+      mbar_init(bar(L::kBarKEmpty + s), 1);
+      mbar_init(bar(L::kBarVFull + s), 1);
+      mbar_init(bar(L::kBarVEmpty + s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar(L::kBarSFull + b), 1);
+      mbar_init(bar(L::kBarSFree + b), kSoftmaxThreads);
+      mbar_init(bar(L::kBarPFull + b), kSoftmaxThreads);
+    }
+    mbar_init(bar(L::kBarODone), 1);
+    mbar_init(bar(L::kBarDrain), 1);
+    mbar_init(bar(L::kBarEpi), kSoftmaxThreads);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(smem_addr(tmem_slot), L::kTmemCols);
+    tmem_relinquish_alloc_permit();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+
+  const uint32_t sQ = base + L::kQOff;
+  auto sK = [&](int s) -> uint32_t { return base + L::kKOff + uint32_t(s) * L::kKVBytes; };
+  auto sV = [&](int s) -> uint32_t { return base + L::kVOff + uint32_t(s) * L::kKVBytes; };
+
+  if (warp == 4) {
+    // ------------------------------------------------------------ producer ----
+    if (lane == 0) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      tma_prefetch_desc(&tmO);
+      mbar_arrive_expect_tx(bar(L::kBarQFull), L::kQBytes);
+      for (int s = 0; s < L::kSlabs; ++s)
+        tma_load_3d(sQ + s * (kBM * 128), &tmQ, bar(L::kBarQFull), s * 64, q0, bh);
+      int k_arms[NS], v_arms[NS];
+#pragma unroll
+      for (int s = 0; s < NS; ++s) k_arms[s] = v_arms[s] = 0;
+      bool ok = true;
+      for (int j = 0; j < nkv; ++j) {
+        const int st = j % NS;
+        const uint32_t ph = (j / NS) & 1;
+        if (j >= NS && !mbar_wait(bar(L::kBarKEmpty + st), ph ^ 1, wc)) { ok = false; break; }
+        mbar_arrive_expect_tx(bar(L::kBarKFull + st), L::kKVBytes);
+        for (int s = 0; s < L::kSlabs; ++s)
+          tma_load_3d(sK(st) + s * (BC * 128), &tmK, bar(L::kBarKFull + st), s * 64, j * BC, bh);
+        ++k_arms[st];
+        if (j >= NS && !mbar_wait(bar(L::kBarVEmpty + st), ph ^ 1, wc)) { ok = false; break; }
+        mbar_arrive_expect_tx(bar(L::kBarVFull + st), L::kKVBytes);
+        for (int s = 0; s < L::kSlabs; ++s)
+          tma_load_3d(sV(st) + s * (BC * 128), &tmV, bar(L::kBarVFull + st), s * 64, j * BC, bh);
+        ++v_arms[st];
+      }
+      if (!ok) {
+        // Let every copy this thread started land before shared memory is released: the
+        // latest armed phase of each full barrier is the last copy issued into that stage.
+        auto drain = [&](uint32_t b, uint32_t parity) {
+          for (uint64_t t0 = global_timer_ns();
+               !mbar_try_wait(b, parity) && global_timer_ns() - t0 < wc.limit_ns;) {
+          }
+        };
+        drain(bar(L::kBarQFull), 0);
+        for (int s = 0; s < NS; ++s) {
+          if (k_arms[s] > 0) drain(bar(L::kBarKFull + s), (k_arms[s] - 1) & 1);
+          if (v_arms[s] > 0) drain(bar(L::kBarVFull + s), (v_arms[s] - 1) & 1);
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 5) {
+    // ---------------------------------------------------------- MMA issuer ----
+    if (lane == 0) {
+      constexpr uint32_t kIdS = idesc_bf16_f32(kBM, BC, 0, 0);  // Q K^T: both K-major
+      constexpr uint32_t kIdO = idesc_bf16_f32(kBM, D, 0, 1);   // P V: V is N(=d)-major
+      auto issue_s = [&](int jj) -> bool {
+        const int st = jj % NS;
+        if (!mbar_wait(bar(L::kBarKFull + st), (jj / NS) & 1, wc)) return false;
+        if (jj >= 2 && !mbar_wait(bar(L::kBarSFree + (jj & 1)), ((jj - 2) >> 1) & 1, wc)) return false;
+        tc_fence_after_sync();
+        const uint32_t d_tmem = tmem + L::kColS + (jj & 1) * BC;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint64_t a = sdesc_sw128(sQ + (kk >> 2) * (kBM * 128) + (kk & 3) * 32, 16, 1024);
+          const uint64_t b = sdesc_sw128(sK(st) + (kk >> 2) * (BC * 128) + (kk & 3) * 32, 16, 1024);
+          mma_ss(d_tmem, a, b, kIdS, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(bar(L::kBarKEmpty + st));
+        mma_commit(bar(L::kBarSFull + (jj & 1)));
+        return true;
+      };
+      bool ok = mbar_wait(bar(L::kBarQFull), 0, wc);
+      if (ok) ok = issue_s(0);
+      for (int j = 0; ok && j < nkv; ++j) {
+        if (j + 1 < nkv && !issue_s(j + 1)) { ok = false; break; }
+        const int st = j % NS;
+        if (!mbar_wait(bar(L::kBarVFull + st), (j / NS) & 1, wc) ||
+            !mbar_wait(bar(L::kBarPFull + (j & 1)), (j >> 1) & 1, wc)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        const uint32_t a_tmem = tmem + L::kColP + (j & 1) * (BC / 2);
+#pragma unroll
+        for (int kk = 0; kk < BC / 16; ++kk) {
+          const uint64_t b = sdesc_sw128(sV(st) + kk * (16 * 128), BC * 128, 1024);
+          mma_ts(tmem + L::kColO, a_tmem + kk * 8, b, kIdO, (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(bar(L::kBarVEmpty + st));
+        mma_commit(bar(L::kBarODone));
+      }
+      // Every MMA issued above must be finished before TMEM is released.
+      mma_commit(bar(L::kBarDrain));
+      for (uint64_t t0 = global_timer_ns();
+           !mbar_try_wait(bar(L::kBarDrain), 0) && global_timer_ns() - t0 < wc.limit_ns;) {
+      }
+    }
+    __syncwarp();
+  } else {
+    // -------------------------------------------------------------- softmax ----
+    const int row = threadIdx.x;                 // 0..127 = TMEM lane
+    const uint32_t lane_off = uint32_t(warp * 32) << 16;
+    const int row_g = q0 + row;
+    const float sl2 = args.scale_log2;
+    float m_run = -INFINITY;  // running max of scale*log2(e)*s
+    float l_run = 0.f;        // running sum of 2^(scaled s - m_run)
+    bool ok = true;
+    for (int j = 0; j < nkv; ++j) {
+      const int b = j & 1;
+      // tcgen05.ld is warp-collective: every wait outcome is made warp-uniform
+      if (!__all_sync(0xffffffffu, mbar_wait(bar(L::kBarSFull + b), (j >> 1) & 1, wc))) { ok = false; break; }
+      tc_fence_after_sync();
+      float s[BC];
+#pragma unroll
+      for (int c = 0; c < BC; c += 32) {
+        uint32_t r[32];
+        tmem_ld32(tmem + lane_off + L::kColS + b * BC + c, r);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) s[c + i] = __uint_as_float(r[i]);
+      }
+      tc_fence_before_sync();
+      mbar_arrive(bar(L::kBarSFree + b));
+
+      // keys kv0 + c are visible for c < lim (sequence tail; causal: key <= query)
+      const int kv0 = j * BC;
+      int lim = N - kv0;
+      if (CAUSAL) lim = min(lim, row_g - kv0 + 1);
+      if (lim < BC) {
+#pragma unroll
+        for (int c = 0; c < BC; ++c)
+          if (c >= lim) s[c] = -INFINITY;
+      }
+      float mx0 = s[0], mx1 = s[1];
+#pragma unroll
+      for (int c = 2; c < BC; c += 2) {
+        mx0 = fmaxf(mx0, s[c]);
+        mx1 = fmaxf(mx1, s[c + 1]);
+      }
+      const float m_new = fmaxf(m_run, fmaxf(mx0, mx1) * sl2);
+      const float alpha = ex2_approx(m_run - m_new);  // 0 on the first tile
+      const bool grew = (j > 0) && (m_new > m_run);
+      m_run = m_new;
+      const float neg_m = -m_new;
+      float sum0 = 0.f, sum1 = 0.f;
+      uint32_t pk[BC / 2];
+#pragma unroll
+      for (int c = 0; c < BC; c += 2) {
+        const float p0 = ex2_approx(fmaf(s[c], sl2, neg_m));
+        const float p1 = ex2_approx(fmaf(s[c + 1], sl2, neg_m));
+        sum0 += p0;
+        sum1 += p1;
+        pk[c / 2] = pack_bf16x2(p0, p1);
+      }
+      l_run = l_run * alpha + (sum0 + sum1);
+      // P_j into its TMEM buffer (its previous reader, P_{j-2} V_{j-2}, finished before
+      // S_j was signalled).
+#pragma unroll
+      for (int c = 0; c < BC / 2; c += 32) {
+        uint32_t w[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) w[i] = pk[c + i];
+        tmem_st32(tmem + lane_off + L::kColP + b * (BC / 2) + c, w);
+      }
+      // Rescale the accumulator when this warp's rows saw a larger maximum.  O holds
+      // P_0..P_{j-1} V; wait until P_{j-1} V_{j-1} has landed.
+      if (__any_sync(0xffffffffu, grew)) {
+        if (!mbar_wait(bar(L::kBarODone), (j - 1) & 1, wc)) { ok = false; }
+        if (__all_sync(0xffffffffu, ok)) {
+          tc_fence_after_sync();
+#pragma unroll 1
+          for (int c = 0; c < D; c += 32) {
+            uint32_t r[32];
+            tmem_ld32(tmem + lane_off + L::kColO + c, r);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+            tmem_st32(tmem + lane_off + L::kColO + c, r);
+          }
+        } else {
+          ok = false;
+        }
+      }
+      tmem_wait_st();
+      tc_fence_before_sync();
+      if (!ok) break;
+      mbar_arrive(bar(L::kBarPFull + b));
+    }
+
+    // ------------------------------------------------------------ epilogue ----
+    const bool fin = ok && __all_sync(0xffffffffu, mbar_wait(bar(L::kBarODone), (nkv - 1) & 1, wc));
+    if (fin) {
+      tc_fence_after_sync();
+      const float inv_l = 1.f / l_run;
+      uint8_t* stage = smem + L::kQOff;  // Q is no longer read by any MMA
+#pragma unroll 1
+      for (int c = 0; c < D; c += 32) {
+        uint32_t r[32];
+        tmem_ld32(tmem + lane_off + L::kColO + c, r);
+        uint32_t w[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          w[i] = pack_bf16x2(__uint_as_float(r[2 * i]) * inv_l, __uint_as_float(r[2 * i + 1]) * inv_l);
+        const int slab = c >> 6;
+        const int chunk0 = (c & 63) >> 3;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int phys = (chunk0 + i) ^ (row & 7);
+          *reinterpret_cast<uint4*>(stage + slab * (kBM * 128) + row * 128 + phys * 16) =
+              make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+        }
+      }
+      fence_proxy_async_smem();
+      if (row_g < N)
+        args.lse[size_t(bh) * N + row_g] = (m_run + lg2_approx(l_run)) * 0.69314718055994531f;
+    }
+    // Every softmax thread arrives (finished or not); thread 0 stores the tile only when all
+    // 128 rows were staged and no wait in the CTA gave up.
+    mbar_arrive(bar(L::kBarEpi));
+    if (threadIdx.x == 0 && fin && mbar_wait(bar(L::kBarEpi), 0, wc) && *abort_flag == 0) {
+      for (int s = 0; s < L::kSlabs; ++s) tma_store_3d(&tmO, sQ + s * (kBM * 128), s * 64, q0, bh);
+      bulk_commit_group();
+      bulk_wait_group_all();
+    }
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, L::kTmemCols);
+  }
+}
+
+template <int D, int BC, int NS, bool CAUSAL>
+cudaError_t launch_cfg(const Maps& m, const FwdArgs& a, cudaStream_t s) {
+  using L = FwdLayout<D, BC, NS>;
+  auto kern = fa_fwd_kernel<D, BC, NS, CAUSAL>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemAlloc);
+  if (e != cudaSuccess) return e;
+  dim3 grid(a.n_q_tiles, a.BH);
+  kern<<<grid, kThreads, L::kSmemAlloc, s>>>(m.q, m.k, m.v, m.o, a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int fwd_kv_tile(int d) { return d == 256 ? 64 : 128; }
+
+cudaError_t launch_fwd(const Maps& m, const FwdArgs& a, int d, bool causal, cudaStream_t s) {
+  switch (d) {
+    case 64:
+      return causal ? launch_cfg<64, 128, 4, true>(m, a, s) : launch_cfg<64, 128, 4, false>(m, a, s);
+    case 128:
+      return causal ? launch_cfg<128, 128, 2, true>(m, a, s) : launch_cfg<128, 128, 2, false>(m, a, s);
+    case 256:
+      return causal ? launch_cfg<256, 64, 2, true>(m, a, s) : launch_cfg<256, 64, 2, false>(m, a, s);
+    default:
+      return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace fa

@@ -1,0 +1,66 @@
+// fa_internal.h -- declarations shared by the host-side C ABI (fa_api.cu) and the kernel
+// translation units.  Not part of the public interface (include/fa.h is).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstddef>
+#include <cstdint>
+
+namespace fa {
+
+// Everything a forward launch needs besides the four tensor maps.
+struct FwdArgs {
+  float* lse;           // [B*H, N] fp32
+  int N;                // sequence length
+  int BH;               // B*H
+  int n_q_tiles;        // ceil(N / 128)
+  float scale_log2;     // scale * log2(e)
+  uint64_t wait_limit_ns;
+  int* err_word;        // per-device error word
+};
+
+// Tensor maps of one [B*H, N, d] bf16 tensor: `rows128` boxes of 64 columns x 128 rows,
+// `rows_kv` boxes of 64 columns x (key tile) rows.
+struct Maps {
+  CUtensorMap q, k, v, o;
+};
+
+// Forward: one launch.  Returns the cudaError_t of the launch.
+cudaError_t launch_fwd(const Maps& maps, const FwdArgs& a, int d, bool causal, cudaStream_t s);
+// Key-tile height the forward kernel uses for head dim d (the K/V tensor-map box height).
+int fwd_kv_tile(int d);
+
+struct BwdArgs {
+  const uint16_t* q;
+  const uint16_t* k;
+  const uint16_t* v;
+  const uint16_t* o;
+  const uint16_t* dout;
+  const float* lse;
+  uint16_t* dq;
+  uint16_t* dk;
+  uint16_t* dv;
+  float* dvec;     // D [B*H, N]
+  float* dq_acc;   // [B*H, N, d] fp32
+  int N;
+  int BH;
+  int d;
+  float scale;
+  float scale_log2;
+  uint64_t wait_limit_ns;
+  int* err_word;
+};
+
+struct BwdMaps {
+  CUtensorMap q, k, v, dout;  // 64-column x 128-row boxes
+};
+
+// Backward: prep, main and dQ-convert launches.  `lse2` and `dvec` describe the fp32
+// [B*H, Np] rows of the workspace (box 128 x 1 x 1); `dk`, `dv` the bf16 outputs.
+// Np = N rounded up to a multiple of 4.
+cudaError_t launch_bwd_all(const BwdMaps& m, const CUtensorMap& lse2, const CUtensorMap& dvec,
+                           const CUtensorMap& dk, const CUtensorMap& dv, const BwdArgs& a,
+                           bool causal, int Np, cudaStream_t s);
+
+}  // namespace fa

@@ -1,0 +1,105 @@
+/*
+ * fa.h -- C ABI of the GB300 (sm_103a) exact-attention library (libfa_gb300.so).
+ *
+ * What the library computes (per batch b and head h, all rows in parallel):
+ *
+ *   S   = scale * Q K^T                 ("FlashAttention算子优化" §2, scale = 1/sqrt(d) there;
+ *                                         any scale > 0 is accepted here)
+ *   causal != 0: key j is hidden from query i when j > i (square, top-left aligned,
+ *                the is_causal=True of the SDPA call in "Flash Attention 原理与实践" §4.2)
+ *   P   = softmax(S) row by row, O = P V ("FlashAttention 与显存" §04)
+ *   LSE = m + ln(l) per row, the natural-log log-sum-exp of the scaled, masked scores
+ *         (the per-row statistics kept for the backward pass, "FlashAttention 与显存" §09)
+ *
+ * computed tile by tile with the streaming softmax of "FlashAttention 与显存" §08, so the
+ * N x N matrices S and P never reach device memory; the backward pass recomputes S and P
+ * block by block from Q, K, V and LSE ("FlashAttention 与显存" §09).
+ *
+ * Common conventions for every entry point:
+ *  - Device pointers.  Every tensor argument is a device pointer owned by the caller
+ *    (the library frees nothing it did not allocate).  Layout is contiguous row-major
+ *    [B, H, N, d] with d innermost for Q, K, V, O, dO, dQ, dK, dV (bfloat16) and [B, H, N]
+ *    for LSE and D (float32).  Every pointer must be 16-byte aligned.
+ *  - Sizes.  B >= 1, H >= 1, N >= 1, B*H <= 65535 * 65535, N <= 2^20; d in {64, 128, 256}.
+ *  - Asynchrony.  Work is enqueued on `stream` (0 = legacy default stream) and the call
+ *    returns without synchronising.  A device-side failure (a bounded wait that gave
+ *    up) is recorded in a per-device error word and reported by fa_status_check().
+ *  - Errors.  Argument problems are detected on the host before anything is launched
+ *    and return FA_ERR_INVALID_ARG / FA_ERR_UNSUPPORTED / FA_ERR_MISALIGNED.  A failed
+ *    launch or CUDA runtime call returns FA_ERR_CUDA.  No entry point aborts or prints.
+ *  - Devices.  Only compute capability 10.3 (GB300) is supported; other devices get
+ *    FA_ERR_UNSUPPORTED.  The library allocates no device memory per call; it keeps one
+ *    small error word per device in static device memory.
+ */
+#ifndef FA_GB300_H_
+#define FA_GB300_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* fa_stream_t; /* same object as cudaStream_t */
+
+typedef enum {
+  FA_OK = 0,
+  FA_ERR_INVALID_ARG = 1, /* null pointer, non-positive size, non-positive or non-finite scale */
+  FA_ERR_UNSUPPORTED = 2, /* head dim not in {64,128,256}, size limit, or not an sm_103 device */
+  FA_ERR_MISALIGNED = 3,  /* a pointer that is not 16-byte aligned */
+  FA_ERR_CUDA = 4,        /* a CUDA runtime / driver call or a kernel launch failed */
+  FA_ERR_TIMEOUT = 5      /* a kernel's bounded wait gave up (reported by fa_status_check) */
+} fa_status;
+
+/*
+ * Forward pass.  q, k, v: bf16 [B,H,N,d] (read only).  o: bf16 [B,H,N,d] (written).
+ * lse: fp32 [B,H,N] (written), natural-log log-sum-exp of the scaled masked scores of each
+ * row.  O is rounded to bf16 to nearest-even from fp32 accumulators.
+ */
+fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                 int B, int H, int N, int d, float scale, int causal, fa_stream_t stream);
+
+/*
+ * Bytes of device workspace fa_bwd needs: D [B,H,N] fp32 followed (at a 256-byte aligned
+ * offset) by the fp32 dQ accumulator [B,H,N,d].  Returns 0 for invalid sizes.
+ */
+size_t fa_bwd_workspace_bytes(int B, int H, int N, int d);
+
+/*
+ * Backward pass.  Inputs q, k, v, o, dout: bf16 [B,H,N,d]; lse: fp32 [B,H,N] as written
+ * by fa_fwd for the same q, k, v, scale and causal flag.  Outputs dq, dk, dv: bf16
+ * [B,H,N,d] (written).  workspace: caller-owned device buffer of at least
+ * fa_bwd_workspace_bytes(B,H,N,d) bytes, 256-byte aligned; its contents on entry do not
+ * matter and on return hold D = rowsum(dO * O) and the fp32 dQ accumulator.
+ * Steps (one stream, no host synchronisation): D and a zeroed dQ accumulator; one pass
+ * over key/value tiles that recomputes S and P and produces dK, dV and accumulates dQ;
+ * dQ conversion to bf16.
+ */
+fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                 const float* lse, void* dq, void* dk, void* dv,
+                 int B, int H, int N, int d, float scale, int causal,
+                 void* workspace, size_t workspace_bytes, fa_stream_t stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the current device's error word.
+ * Returns FA_OK, FA_ERR_TIMEOUT (a kernel's bounded wait gave up; its outputs are
+ * undefined) or FA_ERR_CUDA (the synchronisation itself failed).
+ */
+fa_status fa_status_check(fa_stream_t stream);
+
+/* Static, human-readable name of a status code. */
+const char* fa_status_string(fa_status s);
+
+/*
+ * Upper bound, in nanoseconds, that every device-side wait may spin before the kernel
+ * records FA_ERR_TIMEOUT and exits.  Default 2e9 (2 s); values < 1e6 are raised to 1e6.
+ * Applies to launches made after the call, on every device.  Returns the previous value.
+ */
+uint64_t fa_set_wait_limit_ns(uint64_t ns);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_GB300_H_ */

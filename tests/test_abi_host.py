@@ -1,0 +1,110 @@
+"""Host-side checks of the C ABI: the library builds and loads, exports every entry point
+include/fa.h declares, and rejects bad arguments before anything is launched.  No call here
+reaches a kernel (every one fails validation first), so these run without a GPU."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from exact_attention_96_gb300 import abi, build
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "fa.h")
+FAKE = 0x10000  # 16-byte aligned, never dereferenced: validation fails before any use
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return abi.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fa_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_expected_entry_points():
+    names = declared_functions()
+    assert names == sorted(abi.SIGNATURES), names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    for code, name in [(0, "FA_OK"), (1, "FA_ERR_INVALID_ARG"), (2, "FA_ERR_UNSUPPORTED"),
+                       (3, "FA_ERR_MISALIGNED"), (4, "FA_ERR_CUDA"), (5, "FA_ERR_TIMEOUT")]:
+        assert abi.status_string(code) == name
+    assert abi.status_string(99) == "FA_ERR_UNKNOWN"
+
+
+def fwd(**kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=FAKE, B=1, H=1, N=128, d=64, scale=0.125,
+             causal=0, stream=None)
+    a.update(kw)
+    return abi.fa_fwd(*a.values())
+
+
+def bwd(**kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, do=FAKE, lse=FAKE, dq=FAKE, dk=FAKE, dv=FAKE,
+             B=1, H=1, N=128, d=64, scale=0.125, causal=0, ws=FAKE, ws_bytes=1 << 30, stream=None)
+    a.update(kw)
+    return abi.fa_bwd(*a.values())
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(q=None), abi.FA_ERR_INVALID_ARG),
+    (dict(lse=None), abi.FA_ERR_INVALID_ARG),
+    (dict(B=0), abi.FA_ERR_INVALID_ARG),
+    (dict(H=-1), abi.FA_ERR_INVALID_ARG),
+    (dict(N=0), abi.FA_ERR_INVALID_ARG),
+    (dict(d=96), abi.FA_ERR_UNSUPPORTED),
+    (dict(d=32), abi.FA_ERR_UNSUPPORTED),
+    (dict(B=300, H=300), abi.FA_ERR_UNSUPPORTED),
+    (dict(N=(1 << 20) + 1), abi.FA_ERR_UNSUPPORTED),
+    (dict(scale=0.0), abi.FA_ERR_INVALID_ARG),
+    (dict(scale=-1.0), abi.FA_ERR_INVALID_ARG),
+    (dict(scale=float("nan")), abi.FA_ERR_INVALID_ARG),
+    (dict(scale=float("inf")), abi.FA_ERR_INVALID_ARG),
+    (dict(k=FAKE + 8), abi.FA_ERR_MISALIGNED),
+    (dict(o=FAKE + 2), abi.FA_ERR_MISALIGNED),
+])
+def test_forward_validation(lib, kw, status):
+    assert fwd(**kw) == status
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(do=None), abi.FA_ERR_INVALID_ARG),
+    (dict(ws=None), abi.FA_ERR_INVALID_ARG),
+    (dict(ws_bytes=16), abi.FA_ERR_INVALID_ARG),
+    (dict(d=80), abi.FA_ERR_UNSUPPORTED),
+    (dict(scale=0.0), abi.FA_ERR_INVALID_ARG),
+    (dict(dv=FAKE + 4), abi.FA_ERR_MISALIGNED),
+    (dict(ws=FAKE + 16), abi.FA_ERR_MISALIGNED),
+])
+def test_backward_validation(lib, kw, status):
+    assert bwd(**kw) == status
+
+
+def test_workspace_bytes(lib):
+    def expected(B, H, N, d):
+        r256 = lambda x: (x + 255) // 256 * 256
+        Np = (N + 3) // 4 * 4
+        tiles = (N + 127) // 128
+        # D and LSE*log2(e) rows (fp32, padded to 4), then the fp32 dQ accumulator tiles
+        return 2 * r256(B * H * Np * 4) + B * H * tiles * 128 * d * 4
+    for shape in [(1, 1, 1, 64), (4, 16, 8192, 128), (2, 3, 17, 64), (1, 8, 65536, 64)]:
+        assert abi.fa_bwd_workspace_bytes(*shape) == expected(*shape)
+    assert abi.fa_bwd_workspace_bytes(0, 1, 1, 64) == 0
+    assert abi.fa_bwd_workspace_bytes(1, 1, 1, 48) == 0
+
+
+def test_wait_limit_round_trip(lib):
+    prev = abi.fa_set_wait_limit_ns(5_000_000_000)
+    assert abi.fa_set_wait_limit_ns(10) == 5_000_000_000  # raised to the 1 ms floor on store
+    assert abi.fa_set_wait_limit_ns(prev) == 1_000_000
