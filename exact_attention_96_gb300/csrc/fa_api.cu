@@ -209,6 +209,7 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
   a.dk = static_cast<uint16_t*>(dk);
   a.dv = static_cast<uint16_t*>(dv);
   a.dvec = reinterpret_cast<float*>(ws + w.dvec_off);
+  a.lse2 = reinterpret_cast<float*>(ws + w.lse2_off);
   a.dq_acc = reinterpret_cast<float*>(ws + w.dq_off);
   a.N = N;
   a.BH = BH;

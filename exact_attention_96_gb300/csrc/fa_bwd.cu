@@ -509,7 +509,7 @@ cudaError_t launch_prep_and_convert(const BwdArgs& a, int Np, int n_q_tiles, cud
     constexpr int kRowsPerBlock = 256 / (D / 8);
     const long long rows = (long long)a.BH * n_q_tiles * 128;
     const unsigned grid = unsigned((rows + kRowsPerBlock - 1) / kRowsPerBlock);
-    fa_bwd_prep_kernel<D><<<grid, 256, 0, s>>>(a.o, a.dout, a.lse, a.dvec, a.dvec + (size_t)a.BH * Np,
+    fa_bwd_prep_kernel<D><<<grid, 256, 0, s>>>(a.o, a.dout, a.lse, a.dvec, a.lse2,
                                                a.dq_acc, a.N, Np, n_q_tiles, a.BH);
   } else {
     const long long total = (long long)a.BH * n_q_tiles * 128 * (D / 8);

@@ -41,7 +41,8 @@ struct BwdArgs {
   uint16_t* dq;
   uint16_t* dk;
   uint16_t* dv;
-  float* dvec;     // D [B*H, N]
+  float* dvec;     // D [B*H, Np]
+  float* lse2;     // LSE * log2(e) [B*H, Np]
   float* dq_acc;   // [B*H, N, d] fp32
   int N;
   int BH;

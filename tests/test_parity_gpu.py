@@ -36,6 +36,11 @@ def check_fwd(o, lse, o_ref, lse_ref, what=""):
 
 def check_grad(g, g_ref, what):
     assert np.all(np.isfinite(g)), what
+    if np.linalg.norm(g_ref) < 1e-9 * max(1, g_ref.size):
+        # the exact gradient vanishes (e.g. dQ, dK with a single key): relative error is
+        # undefined, so the bar is an absolute one
+        assert max_abs(g, g_ref) <= 1e-3, (what, max_abs(g, g_ref))
+        return
     assert rel_fro(g, g_ref) <= GRAD_REL_FRO, (what, rel_fro(g, g_ref))
 
 
