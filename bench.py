@@ -1,0 +1,351 @@
+"""Benchmark of exact attention fwd + bwd on GB300 through libfa_gb300.so.
+
+A step is one forward (fa_fwd) and one backward (fa_bwd) pass over the long causal
+language-model shape: B=4, H=16, N=8192, d=128, causal, bf16 inputs drawn iid N(0,1)
+and multiplied by 0.5.  `value` is convention TFLOP/s of the whole step (forward
+4*B*H*N^2*d halved for causal, backward 2.5x that), summed over ranks; inputs (4 x 128 MB)
+exceed the 129 MB L2, so no explicit flush is done between iterations.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+--impl reference times the fp64 CPU oracle (the only reference implementation there is)
+on a bounded sample of the same workload.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "attention fwd / fwd+bwd TFLOPS (bf16) and % of GB300 dense peak; ms per call"
+WORKLOAD = dict(B=4, H=16, N=8192, d=128, causal=True, multiplier=0.5)
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def step_flops(B, H, N, d, causal, **_):
+    fwd = 4.0 * B * H * N * N * d * (0.5 if causal else 1.0)
+    return fwd, 2.5 * fwd
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def config_dict(extra=None):
+    w = WORKLOAD
+    c = {"workload": "long causal LM attention: B=4 H=16 N=8192 d=128 causal, inputs x0.5, fwd+bwd",
+         "global_batch": w["B"], "heads": w["H"], "seq_len": w["N"], "head_dim": w["d"],
+         "causal": w["causal"], "parallelism": "replicas (B*H shards, no collective)",
+         "l2": "inputs exceed L2 (512 MB of bf16 inputs vs 129 MB L2); no flush"}
+    if extra:
+        c.update(extra)
+    return c
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason sampling in the background (200 ms period)."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.device_index = device_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.device_index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+        return False
+
+    def summary(self):
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in getattr(self, "lines", []):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+            except ValueError:
+                continue
+            for name, flag in zip(names, parts[5:9]):
+                if flag.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------- CPU oracle ----
+
+def cpu_oracle_sample(target_s: float = 12.0, max_heads: int = 4):
+    """Times the fp64 oracle (forward + backward of whole heads of the workload) until about
+    `target_s` seconds of CPU work; returns TFLOP/s under the same FLOP convention."""
+    from exact_attention_96_gb300 import inputs as I
+    from oracle import attention as A
+
+    w = WORKLOAD
+    scale = 1.0 / math.sqrt(w["d"])
+    heads, elapsed = 0, 0.0
+    while heads == 0 or (heads < max_heads and elapsed < target_s):
+        q, k, v, do = I.attention_inputs(1, 1, w["N"], w["d"], seed=100 + heads,
+                                         multiplier=w["multiplier"])
+        q, k, v, do = (A.bf16_bits_to_f64(x)[0, 0] for x in (q, k, v, do))
+        t0 = time.perf_counter()
+        A.attention_fwd(q[None, None], k[None, None], v[None, None], scale, w["causal"])
+        A.attention_bwd_head(q, k, v, do, scale, w["causal"])
+        elapsed += time.perf_counter() - t0
+        heads += 1
+    fwd, bwd = step_flops(1, heads, w["N"], w["d"], w["causal"])
+    try:
+        from threadpoolctl import threadpool_info
+        cores = max(int(i.get("num_threads", 0)) for i in threadpool_info()) or os.cpu_count()
+    except Exception:
+        cores = os.cpu_count()
+    return {"value": (fwd + bwd) / elapsed / 1e12, "unit": "TFLOPS", "cores": cores, "kind": "oracle",
+            "sample": f"{heads} of {w['B'] * w['H']} heads (B=1 slices of the workload), fwd+bwd, "
+                      f"fp64 numpy, {elapsed:.1f} s"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    samples = []
+    for i in range(args.warmup + args.steps):
+        r = cpu_oracle_sample(target_s=0.0, max_heads=1)
+        if i >= args.warmup:
+            samples.append(r)
+    value = statistics.median(s["value"] for s in samples)
+    fwd, bwd = step_flops(**WORKLOAD)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": (fwd + bwd) / (value * 1e12) * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config_dict(),
+            "cpu_baseline": {"kind": "oracle", "cores": samples[-1]["cores"], "value": value,
+                             "unit": "TFLOPS", "sample": "each step: " + samples[-1]["sample"]},
+            "e2e": {"value": value, "unit": "TFLOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ GPU arm ----
+
+def run_gpu(args, rank, world, local_rank):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    from exact_attention_96_gb300 import abi, build, inputs as I
+    from exact_attention_96_gb300 import attention as fa
+
+    build.build()
+    abi.load()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    w = WORKLOAD
+    B, H, N, d, causal = w["B"], w["H"], w["N"], w["d"], w["causal"]
+    scale = 1.0 / math.sqrt(d)
+    host = I.attention_inputs(B, H, N, d, seed=1000 * rank, multiplier=w["multiplier"])
+
+    def to_dev(x):
+        return torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).to(dev)
+
+    q, k, v, do = map(to_dev, host)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = torch.empty(fa.workspace_bytes(B, H, N, d), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        fa.forward(q, k, v, causal=causal, scale=scale, out=o, lse=lse)
+        fa.backward(q, k, v, o, do, lse, causal=causal, scale=scale, workspace=ws, grads=(dq, dk, dv))
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    for _ in range(args.warmup):
+        step()
+    if fa.status_check(dev) != abi.FA_OK:
+        raise RuntimeError("device status after warm-up is not FA_OK")
+
+    # Device-timed region: events around every call on the launching stream.
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local_rank) as clocks:
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        for i in range(args.steps):
+            ev[i][0].record(stream)
+            fa.forward(q, k, v, causal=causal, scale=scale, out=o, lse=lse)
+            ev[i][1].record(stream)
+            fa.backward(q, k, v, o, do, lse, causal=causal, scale=scale, workspace=ws, grads=(dq, dk, dv))
+            ev[i][2].record(stream)
+        end.record(stream)
+        torch.cuda.synchronize(dev)
+    barrier()
+    total_ms = start.elapsed_time(end)
+    fwd_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+    bwd_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
+    if fa.status_check(dev) != abi.FA_OK:
+        raise RuntimeError("device status after the timed region is not FA_OK")
+
+    # End-to-end through the public API with host buffers: pinned H2D of q, k, v, dO, the
+    # two calls, D2H of O, LSE, dQ, dK, dV -- every step.
+    pin = [torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).pin_memory() for x in host]
+    outs_host = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (o, lse, dq, dk, dv)]
+    h2d = sum(t.numel() * t.element_size() for t in pin)
+    d2h = sum(t.numel() * t.element_size() for t in outs_host)
+
+    def e2e_step():
+        for src, dst in zip(pin, (q, k, v, do)):
+            dst.copy_(src, non_blocking=True)
+        step()
+        for src, dst in zip((o, lse, dq, dk, dv), outs_host):
+            dst.copy_(src, non_blocking=True)
+
+    e2e_step()
+    barrier()
+    torch.cuda.synchronize(dev)
+    s2, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s2.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e2.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    e2e_ms = s2.elapsed_time(e2)
+
+    def world_max(x):
+        if world == 1:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    total_ms, e2e_ms = world_max(total_ms), world_max(e2e_ms)
+    fwd_ms, bwd_ms = world_max(fwd_ms), world_max(bwd_ms)
+    return dict(total_ms=total_ms, fwd_ms=fwd_ms, bwd_ms=bwd_ms, e2e_ms=e2e_ms, h2d=h2d, d2h=d2h,
+                clocks=clocks.summary())
+
+
+# -------------------------------------------------------------------- main ----
+
+def kernel_traffic(kernel_file: str):
+    """DRAM bytes per launch of the backward main kernel from the committed ncu summary,
+    valid only while the kernel source is unchanged (sha256 recorded beside the figure)."""
+    import hashlib
+    summary = os.path.join(ROOT, "profiles", "bwd_main_c4_traffic.md")
+    src = os.path.join(ROOT, "exact_attention_96_gb300", "csrc", kernel_file)
+    if not os.path.exists(summary):
+        return None
+    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    fields = {}
+    for line in open(summary):
+        if ":" in line and line.startswith("- "):
+            key, val = line[2:].split(":", 1)
+            fields[key.strip()] = val.strip()
+    if fields.get("source_sha256_16") != sha:
+        return None
+    try:
+        return float(fields["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["native", "reference"], default="native")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", 1))
+    local_rank = int(os.environ.get("LOCAL_RANK", 0))
+
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+
+    import torch.distributed as dist
+    if world > 1:
+        dist.init_process_group("nccl", device_id=None)
+    r = run_gpu(args, rank, world, local_rank)
+    if world > 1:
+        dist.destroy_process_group()
+    if rank != 0:
+        return
+
+    fwd_f, bwd_f = step_flops(**WORKLOAD)
+    ms = r["total_ms"] / args.steps
+    value = world * (fwd_f + bwd_f) / (ms * 1e-3) / 1e12
+    peaks, src = load_peaks()
+    sustained = peaks.get("bf16_tflops_sustained") or peaks["bf16_tflops"]
+    bwd_tf = bwd_f / (r["bwd_ms"] * 1e-3) / 1e12
+    fwd_tf = fwd_f / (r["fwd_ms"] * 1e-3) / 1e12
+    e2e_ms = r["e2e_ms"] / args.steps
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) x0.5, bf16)",
+        "config": config_dict(),
+        "fwd": {"ms": r["fwd_ms"], "tflops": fwd_tf, "frac_of_sustained_peak": fwd_tf / sustained,
+                "frac_of_burst_peak": fwd_tf / peaks["bf16_tflops"]},
+        "bwd": {"ms": r["bwd_ms"], "tflops": bwd_tf, "frac_of_sustained_peak": bwd_tf / sustained,
+                "frac_of_burst_peak": bwd_tf / peaks["bf16_tflops"]},
+        "roofline": {"bound": "tensor", "kernel": "fa_bwd call (main kernel + prep + dq convert)",
+                     "achieved": bwd_tf, "peak": sustained, "unit": "TFLOP/s",
+                     "frac": bwd_tf / sustained, "peak_source": f"{src} bf16 sustained",
+                     "traffic": kernel_traffic("fa_bwd.cu")},
+        "e2e": {"value": world * (fwd_f + bwd_f) / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOPS",
+                "ms_per_step": e2e_ms, "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
+        "gpu_launches": 4 * args.steps,
+        "clocks": r["clocks"],
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_oracle_sample()
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()
