@@ -32,6 +32,9 @@ SIGNATURES = {
                         _c_void_p, _c_void_p, _c_void_p,
                         _c_int, _c_int, _c_int, _c_int, _c_float, _c_int,
                         _c_void_p, _c_size_t, _c_void_p]),
+    "fa_bwd_noalloc": (_c_int, [_c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_void_p,
+                                _c_void_p, _c_void_p, _c_void_p,
+                                _c_int, _c_int, _c_int, _c_int, _c_float, _c_int, _c_void_p]),
     "fa_status_check": (_c_int, [_c_void_p]),
     "fa_status_string": (ctypes.c_char_p, [_c_int]),
     "fa_set_wait_limit_ns": (ctypes.c_uint64, [ctypes.c_uint64]),
@@ -83,6 +86,10 @@ def fa_bwd_workspace_bytes(B, H, N, d) -> int:
 def fa_bwd(q, k, v, o, do, lse, dq, dk, dv, B, H, N, d, scale, causal, ws, ws_bytes, stream) -> int:
     return load().fa_bwd(q, k, v, o, do, lse, dq, dk, dv, B, H, N, d, scale, int(causal),
                          ws, ws_bytes, stream)
+
+
+def fa_bwd_noalloc(q, k, v, o, do, lse, dq, dk, dv, B, H, N, d, scale, causal, stream) -> int:
+    return load().fa_bwd_noalloc(q, k, v, o, do, lse, dq, dk, dv, B, H, N, d, scale, int(causal), stream)
 
 
 def fa_status_check(stream) -> int:

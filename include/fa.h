@@ -29,7 +29,8 @@
  *    launch or CUDA runtime call returns FA_ERR_CUDA.  No entry point aborts or prints.
  *  - Devices.  Only compute capability 10.3 (GB300) is supported; other devices get
  *    FA_ERR_UNSUPPORTED.  The library allocates no device memory per call; it keeps one
- *    small error word per device in static device memory.
+ *    small error word per device in static device memory, plus the fixed scratch array of
+ *    fa_bwd_noalloc (below).
  */
 #ifndef FA_GB300_H_
 #define FA_GB300_H_
@@ -80,6 +81,36 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
                  const float* lse, void* dq, void* dk, void* dv,
                  int B, int H, int N, int d, float scale, int causal,
                  void* workspace, size_t workspace_bytes, fa_stream_t stream);
+
+/*
+ * Size in bytes of the static scratch array used by fa_bwd_noalloc (64 MiB per device).
+ */
+#define FA_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
+
+/*
+ * fa_bwd_noalloc -- the backward pass of fa_bwd for callers that cannot allocate device
+ * memory (the pages have no counterpart: this is a deployment convenience).  Examples of
+ * such callers: code running while a stream is being captured into a CUDA graph, where
+ * cudaMalloc is not allowed; latency-critical code that must not hit the implicit device
+ * synchronisation of cudaMalloc / cudaFree; embedders whose device memory belongs to an
+ * allocator they cannot reach from here.
+ *
+ * Arguments and results are those of fa_bwd without the workspace: the workspace is a
+ * file-scope static device array of FA_NOALLOC_SCRATCH_BYTES, held by every device that
+ * loads the library until the process exits.  Nothing is allocated or freed by this call.
+ *  - Limit: returns FA_ERR_UNSUPPORTED, launching nothing, when
+ *    fa_bwd_workspace_bytes(B,H,N,d) > FA_NOALLOC_SCRATCH_BYTES (for d = 128 that is
+ *    about B*H*N <= 129,000 rows); use fa_bwd with a caller workspace beyond that.
+ *  - Set-up: the first call on a device, with that device current, looks up the array's
+ *    device address (cudaGetSymbolAddress) and caches it; make that first call before any
+ *    stream capture starts.
+ *  - Sharing: all calls on a device use the same array.  Calls that overlap on the GPU
+ *    (other streams, unordered host threads) race on it and give undefined results.  The
+ *    array keeps the last call's contents; the pass clears what must start at zero.
+ */
+fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
+                         const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                         int B, int H, int N, int d, float scale, int causal, fa_stream_t stream);
 
 /*
  * Synchronises `stream`, then reads and clears the current device's error word.
