@@ -41,6 +41,7 @@ __all__ = [
     "attention_bwd",
     "attention_bwd_head",
     "attention_bwd_rows",
+    "attention_bwd_key_columns",
 ]
 
 
@@ -175,3 +176,34 @@ def attention_bwd_rows(q_head, k_head, v_head, do_head, scale: float, causal: bo
     drow = np.sum(do * o, axis=1)
     ds = p * (dp - drow[:, None])
     return scale * (ds @ k), drow
+
+
+def attention_bwd_key_columns(q_head, k_head, v_head, do_head, scale: float, causal: bool,
+                              keys, row_chunk: int = 512):
+    """dK and dV rows of selected keys of one head, exactly from the definition.
+
+    dV_j = sum_i P_ij dO_i and dK_j = scale * sum_i dS_ij Q_i need column j of P and dS over
+    every query row i, so every row's softmax (and O_i for D_i) is formed in chunks of
+    rows; only the selected key columns are kept.
+    """
+    keys = np.asarray(keys, dtype=np.int64)
+    q = np.asarray(q_head, np.float64)
+    k = np.asarray(k_head, np.float64)
+    v = np.asarray(v_head, np.float64)
+    do = np.asarray(do_head, np.float64)
+    N = q.shape[0]
+    dk = np.zeros((keys.size, k.shape[1]))
+    dv = np.zeros((keys.size, v.shape[1]))
+    v_sel = v[keys]
+    for r0 in range(0, N, row_chunk):
+        r1 = min(N, r0 + row_chunk)
+        rows = np.arange(r0, r1)
+        s = scores(q[r0:r1], k, scale, causal, rows)
+        p, _, _ = _softmax_rows(s)
+        o = p @ v
+        drow = np.sum(do[r0:r1] * o, axis=1)
+        p_sel = p[:, keys]
+        ds_sel = p_sel * (do[r0:r1] @ v_sel.T - drow[:, None])
+        dv += p_sel.T @ do[r0:r1]
+        dk += scale * (ds_sel.T @ q[r0:r1])
+    return dk, dv

@@ -141,6 +141,28 @@ def test_sampled_rows_match_whole_tensor():
         assert np.max(np.abs(d_r - dvec[rows])) < 1e-13
 
 
+def test_sampled_key_columns_match_whole_head():
+    N, d = 90, 8
+    q, k, v, do = (rnd((N, d), s) for s in (25, 26, 27, 28))
+    keys = np.array([0, 5, 44, 89])
+    for causal in (False, True):
+        _, dk, dv, _ = A.attention_bwd_head(q, k, v, do, 0.3, causal, row_chunk=32)
+        dk_c, dv_c = A.attention_bwd_key_columns(q, k, v, do, 0.3, causal, keys, row_chunk=17)
+        assert np.max(np.abs(dk_c - dk[keys])) < 1e-13
+        assert np.max(np.abs(dv_c - dv[keys])) < 1e-13
+
+
+def test_gradient_sums_over_keys():
+    # Rows of P sum to one and rows of dS sum to zero, so summed over keys dV equals the
+    # sum of dO over queries and dK sums to zero -- identities usable at any size.
+    N, d = 40, 6
+    q, k, v, do = (rnd((N, d), s) for s in (29, 30, 31, 32))
+    for causal in (False, True):
+        _, dk, dv, _ = A.attention_bwd_head(q, k, v, do, 0.5, causal)
+        assert np.max(np.abs(dv.sum(axis=0) - do.sum(axis=0))) < 1e-12
+        assert np.max(np.abs(dk.sum(axis=0))) < 1e-12
+
+
 # ------------------------------------------------------- finite differences ---
 
 @pytest.mark.parametrize("causal", [False, True])
