@@ -123,7 +123,11 @@ fa_bwd_dq_kernel(const float* __restrict__ dq_acc, uint16_t* __restrict__ dq, in
 // ------------------------------------------------------------------ main ----
 
 constexpr int kTile = 128;  // keys per CTA and queries per inner step
-constexpr int kMainThreads = 320;
+constexpr int kMainThreads = 448;
+constexpr int kRowThreads = 256;     // warps 0-7: key rows, split into two column halves
+constexpr int kDrainWarp0 = 8;       // warps 8-11: dQ drain
+constexpr int kProducerWarp = 12;
+constexpr int kMmaWarp = 13;
 
 template <int D, int NS>
 struct BwdLayout {
@@ -150,13 +154,13 @@ struct BwdLayout {
   static constexpr int kBarDQDrained = kBarDQFull + 1;
   static constexpr int kBarDSFree = kBarDQDrained + 1;
   static constexpr int kBarAccDone = kBarDSFree + 1;
-  static constexpr int kBarEpi = kBarAccDone + 1;
-  static constexpr int kBarDrain = kBarEpi + 1;
+  static constexpr int kBarEpi = kBarAccDone + 1;   // 2: one per column half
+  static constexpr int kBarDrain = kBarEpi + 2;
   static constexpr int kNumBars = kBarDrain + 1;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kBytes = kMiscOff + 16;
   // TMEM columns
-  static constexpr int kColS = 0;
+  static constexpr int kColS = 0;      // S^T, then P^T (bf16 pairs) packed inside it
   static constexpr int kColDP = 128;   // dP^T, then the dQ tile
   static constexpr int kColDV = 256;
   static constexpr int kColDK = 256 + D;
@@ -201,23 +205,24 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
     mbar_init(bar(L::kBarKV), 1);
     for (int s = 0; s < NS; ++s) {
       mbar_init(bar(L::kBarQFull + s), 1);
-      mbar_init(bar(L::kBarQEmpty + s), 128 + 1);  // key-row warps + MMA commit
+      mbar_init(bar(L::kBarQEmpty + s), kRowThreads + 1);  // key-row warps + MMA commit
     }
     mbar_init(bar(L::kBarSFull), 1);
     mbar_init(bar(L::kBarDPFull), 1);
-    mbar_init(bar(L::kBarPReady), 128);
-    mbar_init(bar(L::kBarDSReady), 128);
+    mbar_init(bar(L::kBarPReady), kRowThreads);
+    mbar_init(bar(L::kBarDSReady), kRowThreads);
     mbar_init(bar(L::kBarDVDone), 1);
     mbar_init(bar(L::kBarDQFull), 1);
     mbar_init(bar(L::kBarDQDrained), 128);
     mbar_init(bar(L::kBarDSFree), 1);
     mbar_init(bar(L::kBarAccDone), 1);
-    mbar_init(bar(L::kBarEpi), 128);
+    mbar_init(bar(L::kBarEpi + 0), 128);
+    mbar_init(bar(L::kBarEpi + 1), 128);
     mbar_init(bar(L::kBarDrain), 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 9) {
+  if (warp == kMmaWarp) {
     tmem_alloc(smem_addr(tmem_slot), L::kTmemCols);
     tmem_relinquish_alloc_permit();
   }
@@ -230,7 +235,7 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
   auto sQ = [&](int s) -> uint32_t { return base + L::kQOff + uint32_t(s) * L::kTileBytes; };
   auto sdO = [&](int s) -> uint32_t { return base + L::kdOOff + uint32_t(s) * L::kTileBytes; };
 
-  if (warp == 8) {
+  if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer ----
     if (lane == 0) {
       tma_prefetch_desc(&tmQ);
@@ -272,18 +277,17 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
       }
     }
     __syncwarp();
-  } else if (warp == 9) {
+  } else if (warp == kMmaWarp) {
     // ---------------------------------------------------------- MMA issuer ----
+    // Order per query tile i:  dV_i | S_{i+1} | dK_i, dQ_i | dP_{i+1}
+    // so that the key-row warps turn S_{i+1} into P_{i+1} while dK_i and dQ_i run.
     if (lane == 0) {
       constexpr uint32_t kIdSq = idesc_bf16_f32(128, 128, 0, 0);  // S^T, dP^T
       constexpr uint32_t kIdAcc = idesc_bf16_f32(128, D, 0, 1);   // dV, dK: B N-major
       constexpr uint32_t kIdDQ = idesc_bf16_f32(128, D, 1, 1);    // dQ: A (dS) M-major, B N-major
-      bool ok = mbar_wait(bar(L::kBarKV), 0, wc);
-      for (int it = 0; ok && it < n_it; ++it) {
+      auto issue_s = [&](int it) -> bool {
         const int st = it % NS;
-        const uint32_t ph = it & 1;
-        if (!mbar_wait(bar(L::kBarQFull + st), (it / NS) & 1, wc)) { ok = false; break; }
-        if (it > 0 && !mbar_wait(bar(L::kBarDVDone), ph ^ 1, wc)) { ok = false; break; }
+        if (!mbar_wait(bar(L::kBarQFull + st), (it / NS) & 1, wc)) return false;
         tc_fence_after_sync();
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
@@ -292,7 +296,10 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                  kIdSq, kk > 0 ? 1u : 0u);
         }
         mma_commit(bar(L::kBarSFull));
-        if (it > 0 && !mbar_wait(bar(L::kBarDQDrained), ph ^ 1, wc)) { ok = false; break; }
+        return true;
+      };
+      auto issue_dp = [&](int it) {
+        const int st = it % NS;
         tc_fence_after_sync();
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
@@ -301,16 +308,29 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                  kIdSq, kk > 0 ? 1u : 0u);
         }
         mma_commit(bar(L::kBarDPFull));
+      };
+      bool ok = mbar_wait(bar(L::kBarKV), 0, wc) && issue_s(0);
+      if (ok) issue_dp(0);
+      for (int it = 0; ok && it < n_it; ++it) {
+        const int st = it % NS;
+        const uint32_t ph = it & 1;
         if (!mbar_wait(bar(L::kBarPReady), ph, wc)) { ok = false; break; }
         tc_fence_after_sync();
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk) {
-          mma_ts(tmem + L::kColDV, tmem + L::kColS + kk * 8,
+          // P^T of queries 16kk..16kk+15 sits in 8 columns of its half's S^T range
+          mma_ts(tmem + L::kColDV, tmem + L::kColS + (kk >> 2) * 64 + (kk & 3) * 8,
                  sdesc_sw128(sdO(st) + kk * (16 * 128), kTile * 128, 1024), kIdAcc,
                  (it > 0 || kk > 0) ? 1u : 0u);
         }
         mma_commit(bar(L::kBarDVDone));
         if (!mbar_wait(bar(L::kBarDSReady), ph, wc)) { ok = false; break; }
+        // S_{i+1} overwrites P^T_i: the dV product reading it must have completed, and the
+        // key-row warps have finished reading it (they published dS_i after that).
+        if (it + 1 < n_it && !(mbar_wait(bar(L::kBarDVDone), ph, wc) && issue_s(it + 1))) {
+          ok = false;
+          break;
+        }
         tc_fence_after_sync();
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk) {
@@ -327,6 +347,11 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
         mma_commit(bar(L::kBarDQFull));
         mma_commit(bar(L::kBarDSFree));
         mma_commit(bar(L::kBarQEmpty + st));
+        // dP_{i+1} overwrites the dQ_i tile: wait until the drain warps have read it.
+        if (it + 1 < n_it) {
+          if (!mbar_wait(bar(L::kBarDQDrained), ph, wc)) { ok = false; break; }
+          issue_dp(it + 1);
+        }
       }
       if (ok) mma_commit(bar(L::kBarAccDone));
       mma_commit(bar(L::kBarDrain));
@@ -335,10 +360,15 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
       }
     }
     __syncwarp();
-  } else if (warp < 4) {
+  } else if (warp < 8) {
     // ------------------------------------------------------------ key rows ----
-    const int t = threadIdx.x;  // key row within the tile = TMEM lane
-    const uint32_t lane_off = uint32_t(warp * 32) << 16;
+    // Two warpgroups split the 128 query columns of each tile: half h owns queries
+    // [64h, 64h + 64).  P^T for query q (bf16 pairs) is packed into TMEM column
+    // 64*(q/64) + (q%64)/2, inside the S^T columns the same warpgroup has already read.
+    const int t = threadIdx.x & 127;       // key row within the tile = TMEM lane
+    const int half = threadIdx.x >> 7;     // 0 or 1
+    const int c0 = half * 64;
+    const uint32_t lane_off = uint32_t((warp & 3) * 32) << 16;
     const int key = k0 + t;
     const float sl2 = args.scale_log2;
     bool ok = true;
@@ -347,28 +377,34 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
       const uint32_t ph = it & 1;
       const int q0 = (it_first + it) * kTile;
       const bool edge = (CAUSAL && it == 0) || (q0 + kTile > N);  // any masking in this tile
-      const float* lse2 = reinterpret_cast<const float*>(smem + L::kLseOff + st * 512);
-      const float* dv = reinterpret_cast<const float*>(smem + L::kDOff + st * 512);
+      const float* lse2 = reinterpret_cast<const float*>(smem + L::kLseOff + st * 512) + c0;
+      const float* dvv = reinterpret_cast<const float*>(smem + L::kDOff + st * 512) + c0;
       // phase 1: P^T
       if (!__all_sync(0xffffffffu, mbar_wait(bar(L::kBarSFull), ph, wc))) { ok = false; break; }
       tc_fence_after_sync();
-#pragma unroll 1
-      for (int c = 0; c < kTile; c += 32) {
+#pragma unroll
+      for (int cc = 0; cc < 64; cc += 32) {
         uint32_t r[32];
-        tmem_ld32(tmem + lane_off + L::kColS + c, r);
+        tmem_ld32(tmem + lane_off + L::kColS + c0 + cc, r);
+        float lv[32];
+#pragma unroll
+        for (int e = 0; e < 32; e += 4) {
+          const float4 x = *reinterpret_cast<const float4*>(lse2 + cc + e);
+          lv[e] = x.x; lv[e + 1] = x.y; lv[e + 2] = x.z; lv[e + 3] = x.w;
+        }
         uint32_t w[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
-          float p0 = ex2_approx(fmaf(__uint_as_float(r[e]), sl2, -lse2[c + e]));
-          float p1 = ex2_approx(fmaf(__uint_as_float(r[e + 1]), sl2, -lse2[c + e + 1]));
+          float p0 = ex2_approx(fmaf(__uint_as_float(r[e]), sl2, -lv[e]));
+          float p1 = ex2_approx(fmaf(__uint_as_float(r[e + 1]), sl2, -lv[e + 1]));
           if (edge) {
-            const int qa = q0 + c + e;
+            const int qa = q0 + c0 + cc + e;
             if (qa >= N || (CAUSAL && qa < key)) p0 = 0.f;
             if (qa + 1 >= N || (CAUSAL && qa + 1 < key)) p1 = 0.f;
           }
           w[e / 2] = pack_bf16x2(p0, p1);
         }
-        tmem_st16(tmem + lane_off + L::kColS + c / 2, w);
+        tmem_st16(tmem + lane_off + L::kColS + c0 + cc / 2, w);
       }
       tmem_wait_st();
       tc_fence_before_sync();
@@ -378,33 +414,37 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
       if (it > 0) got = got && mbar_wait(bar(L::kBarDSFree), ph ^ 1, wc);
       if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
       tc_fence_after_sync();
-#pragma unroll 1
-      for (int c = 0; c < kTile; c += 32) {
+#pragma unroll
+      for (int cc = 0; cc < 64; cc += 32) {
         uint32_t r[32];
         uint32_t pr[16];
-        tmem_ld32(tmem + lane_off + L::kColDP + c, r);
-        tmem_ld16(tmem + lane_off + L::kColS + c / 2, pr);
+        tmem_ld32(tmem + lane_off + L::kColDP + c0 + cc, r);
+        tmem_ld16(tmem + lane_off + L::kColS + c0 + cc / 2, pr);
+        float dl[32];
+#pragma unroll
+        for (int e = 0; e < 32; e += 4) {
+          const float4 x = *reinterpret_cast<const float4*>(dvv + cc + e);
+          dl[e] = x.x; dl[e + 1] = x.y; dl[e + 2] = x.z; dl[e + 3] = x.w;
+        }
         uint32_t w[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
           const float p0 = __uint_as_float(pr[e / 2] << 16);
           const float p1 = __uint_as_float(pr[e / 2] & 0xFFFF0000u);
-          float ds0 = p0 * (__uint_as_float(r[e]) - dv[c + e]);
-          float ds1 = p1 * (__uint_as_float(r[e + 1]) - dv[c + e + 1]);
+          float ds0 = p0 * (__uint_as_float(r[e]) - dl[e]);
+          float ds1 = p1 * (__uint_as_float(r[e + 1]) - dl[e + 1]);
           if (edge) {
-            const int qa = q0 + c + e;
+            const int qa = q0 + c0 + cc + e;
             if (qa >= N) ds0 = 0.f;
             if (qa + 1 >= N) ds1 = 0.f;
           }
           w[e / 2] = pack_bf16x2(ds0, ds1);
         }
-        // dS^T row t, queries c..c+31 -> 128-byte swizzled [2 slabs x 128 rows x 128 B]
-        const int slab = c >> 6;
-        const int chunk0 = (c & 63) >> 3;
+        // dS^T row t, queries c0+cc .. c0+cc+31 -> slab `half`, 16-byte chunks cc/8 ..
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          const int phys = (chunk0 + i) ^ (t & 7);
-          *reinterpret_cast<uint4*>(smem + L::kdSOff + slab * (kTile * 128) + t * 128 + phys * 16) =
+          const int phys = ((cc >> 3) + i) ^ (t & 7);
+          *reinterpret_cast<uint4*>(smem + L::kdSOff + half * (kTile * 128) + t * 128 + phys * 16) =
               make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
         }
       }
@@ -413,79 +453,78 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
       mbar_arrive(bar(L::kBarDSReady));
       mbar_arrive(bar(L::kBarQEmpty + st));
     }
-    // epilogue: dV then dK (scaled), staged in shared memory, TMA-stored
-    bool fin = ok && __all_sync(0xffffffffu, mbar_wait(bar(L::kBarAccDone), 0, wc));
+    // epilogue: half 0 stores dV, half 1 stores dK (scaled), each staged in a free stage-0
+    // tile and written by one TMA store per 64-column slab
+    const bool fin = ok && __all_sync(0xffffffffu, mbar_wait(bar(L::kBarAccDone), 0, wc));
+    const uint32_t col = half == 0 ? L::kColDV : L::kColDK;
+    const float mul = half == 0 ? 1.f : args.scale;
+    uint8_t* stage = smem + (half == 0 ? L::kQOff : L::kdOOff);
     if (fin) {
       tc_fence_after_sync();
-      for (int which = 0; which < 2; ++which) {
-        const uint32_t col = which == 0 ? L::kColDV : L::kColDK;
-        const float mul = which == 0 ? 1.f : args.scale;
-        uint8_t* stage = smem + (which == 0 ? L::kQOff : L::kdOOff);  // stage 0 buffers, free now
 #pragma unroll 1
-        for (int c = 0; c < D; c += 32) {
-          uint32_t r[32];
-          tmem_ld32(tmem + lane_off + col + c, r);
-          uint32_t w[16];
+      for (int c = 0; c < D; c += 32) {
+        uint32_t r[32];
+        tmem_ld32(tmem + lane_off + col + c, r);
+        uint32_t w[16];
 #pragma unroll
-          for (int e = 0; e < 16; ++e)
-            w[e] = pack_bf16x2(__uint_as_float(r[2 * e]) * mul, __uint_as_float(r[2 * e + 1]) * mul);
-          const int slab = c >> 6;
-          const int chunk0 = (c & 63) >> 3;
+        for (int e = 0; e < 16; ++e)
+          w[e] = pack_bf16x2(__uint_as_float(r[2 * e]) * mul, __uint_as_float(r[2 * e + 1]) * mul);
+        const int slab = c >> 6;
+        const int chunk0 = (c & 63) >> 3;
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int phys = (chunk0 + i) ^ (t & 7);
-            *reinterpret_cast<uint4*>(stage + slab * (kTile * 128) + t * 128 + phys * 16) =
-                make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
-          }
+        for (int i = 0; i < 4; ++i) {
+          const int phys = (chunk0 + i) ^ (t & 7);
+          *reinterpret_cast<uint4*>(stage + slab * (kTile * 128) + t * 128 + phys * 16) =
+              make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
         }
       }
       fence_proxy_async_smem();
     }
-    mbar_arrive(bar(L::kBarEpi));
-    if (t == 0 && fin) {
-      if (mbar_wait(bar(L::kBarEpi), 0, wc) && *abort_flag == 0) {
-        for (int s = 0; s < L::kSlabs; ++s) {
-          tma_store_3d(&tmdV, sQ(0) + s * (kTile * 128), s * 64, k0, bh);
-          tma_store_3d(&tmdK, sdO(0) + s * (kTile * 128), s * 64, k0, bh);
-        }
-        bulk_commit_group();
-        bulk_wait_group_all();
-      }
+    mbar_arrive(bar(L::kBarEpi + half));
+    if (t == 0 && fin && mbar_wait(bar(L::kBarEpi + half), 0, wc) && *abort_flag == 0) {
+      const CUtensorMap* map = half == 0 ? &tmdV : &tmdK;
+      const uint32_t src = half == 0 ? sQ(0) : sdO(0);
+      for (int s = 0; s < L::kSlabs; ++s) tma_store_3d(map, src + s * (kTile * 128), s * 64, k0, bh);
+      bulk_commit_group();
+      bulk_wait_group_all();
     }
-  } else {
-    // --------------------------------------------------------- query rows ----
-    const int t = threadIdx.x - 128;
-    const uint32_t lane_off = uint32_t((warp - 4) * 32) << 16;
-    const int n_tiles_total = n_q_tiles;
+  } else if (warp < kProducerWarp) {
+    // --------------------------------------------------------- dQ drain ----
+    const int t = threadIdx.x - kDrainWarp0 * 32;   // query row within the tile = TMEM lane
+    const uint32_t lane_off = uint32_t((warp & 3) * 32) << 16;
     for (int it = 0; it < n_it; ++it) {
       const int qt = it_first + it;
       if (!__all_sync(0xffffffffu, mbar_wait(bar(L::kBarDQFull), it & 1, wc))) break;
       tc_fence_after_sync();
-      float4* dst = reinterpret_cast<float4*>(args.dq_acc + ((size_t)bh * n_tiles_total + qt) * 128 * D);
-      uint32_t r[D];
+      float4* dst = reinterpret_cast<float4*>(args.dq_acc + ((size_t)bh * n_q_tiles + qt) * 128 * D);
+      const bool live = qt * kTile + t < N;
 #pragma unroll
-      for (int c = 0; c < D; c += 32) {
-        uint32_t chunk[32];
-        tmem_ld32(tmem + lane_off + L::kColDP + c, chunk);
+      for (int h = 0; h < D / 64; ++h) {
+        uint32_t a[32], b[32];
+        tmem_ld32(tmem + lane_off + L::kColDP + 64 * h, a);
+        tmem_ld32(tmem + lane_off + L::kColDP + 64 * h + 32, b);
+        if (h == D / 64 - 1) {  // every column of this dQ tile is in registers
+          tc_fence_before_sync();
+          mbar_arrive(bar(L::kBarDQDrained));
+        }
+        if (live) {
 #pragma unroll
-        for (int e = 0; e < 32; ++e) r[c + e] = chunk[e];
-      }
-      // the whole dQ row is in registers: hand the TMEM columns back to the MMA warp
-      tc_fence_before_sync();
-      mbar_arrive(bar(L::kBarDQDrained));
-      if (qt * kTile + t < N) {
-#pragma unroll
-        for (int g = 0; g < D / 4; ++g)
-          atomicAdd(dst + g * 128 + t,
-                    make_float4(__uint_as_float(r[4 * g]), __uint_as_float(r[4 * g + 1]),
-                                __uint_as_float(r[4 * g + 2]), __uint_as_float(r[4 * g + 3])));
+          for (int g = 0; g < 8; ++g) {
+            atomicAdd(dst + (16 * h + g) * 128 + t,
+                      make_float4(__uint_as_float(a[4 * g]), __uint_as_float(a[4 * g + 1]),
+                                  __uint_as_float(a[4 * g + 2]), __uint_as_float(a[4 * g + 3])));
+            atomicAdd(dst + (16 * h + 8 + g) * 128 + t,
+                      make_float4(__uint_as_float(b[4 * g]), __uint_as_float(b[4 * g + 1]),
+                                  __uint_as_float(b[4 * g + 2]), __uint_as_float(b[4 * g + 3])));
+          }
+        }
       }
     }
   }
 
   tc_fence_before_sync();
   __syncthreads();
-  if (warp == 9) {
+  if (warp == kMmaWarp) {
     tc_fence_after_sync();
     tmem_dealloc(tmem, L::kTmemCols);
   }

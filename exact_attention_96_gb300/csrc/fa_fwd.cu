@@ -62,7 +62,8 @@ struct FwdLayout {
   static constexpr int kBarODone = kBarPFull + 2;
   static constexpr int kBarDrain = kBarODone + 1;
   static constexpr int kBarEpi = kBarDrain + 1;
-  static constexpr int kNumBars = kBarEpi + 1;
+  static constexpr int kBarOFinal = kBarEpi + 1;  // single use: every P V product has landed
+  static constexpr int kNumBars = kBarOFinal + 1;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // tmem slot, abort flag
   static constexpr int kBytes = kMiscOff + 16;
   static constexpr int kSmemAlloc = kBytes + 1024;  // slack for the 1024-byte alignment
@@ -118,6 +119,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     mbar_init(bar(L::kBarODone), 1);
     mbar_init(bar(L::kBarDrain), 1);
     mbar_init(bar(L::kBarEpi), kSoftmaxThreads);
+    mbar_init(bar(L::kBarOFinal), 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -219,6 +221,9 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         mma_commit(bar(L::kBarVEmpty + st));
         mma_commit(bar(L::kBarODone));
       }
+      // The epilogue cannot use the per-tile O barrier: the softmax warps may run up to two
+      // P V products ahead of the tensor core, and a parity wait cannot tell phases two apart.
+      if (ok) mma_commit(bar(L::kBarOFinal));
       // Every MMA issued above must be finished before TMEM is released.
       mma_commit(bar(L::kBarDrain));
       for (uint64_t t0 = global_timer_ns();
@@ -316,7 +321,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     }
 
     // ------------------------------------------------------------ epilogue ----
-    const bool fin = ok && __all_sync(0xffffffffu, mbar_wait(bar(L::kBarODone), (nkv - 1) & 1, wc));
+    const bool fin = ok && __all_sync(0xffffffffu, mbar_wait(bar(L::kBarOFinal), 0, wc));
     if (fin) {
       tc_fence_after_sync();
       const float inv_l = 1.f / l_run;

@@ -142,3 +142,18 @@ def test_backward_workspace_reuse_is_deterministic_up_to_atomics():
     assert fa.status_check() == abi.FA_OK
     assert torch.equal(g1[1], g2[1]) and torch.equal(g1[2], g2[2])
     assert rel_fro(to_f64(g1[0]), to_f64(g2[0])) < 1e-3
+
+
+@pytest.mark.parametrize("B,H,N,d,causal", [(2, 8, 4096, 256, False), (1, 4, 4096, 128, False),
+                                            (1, 4, 8192, 64, True)])
+def test_forward_bitwise_repeatable(B, H, N, d, causal):
+    # The forward has no atomics: the same inputs must give bitwise identical O and LSE.
+    # (A wait that could observe the tensor core two products behind once let the output
+    # tile be read early at d = 256, where the softmax runs ahead of the wide P V products.)
+    _, (tq, tk, tv, _) = device_inputs(B, H, N, d, seed=9, grad=False)
+    o0, l0 = fa.forward(tq, tk, tv, causal=causal)
+    o0, l0 = o0.clone(), l0.clone()
+    for _ in range(3):
+        o, l = fa.forward(tq, tk, tv, causal=causal)
+        assert torch.equal(o, o0) and torch.equal(l, l0)
+    assert fa.status_check() == abi.FA_OK
