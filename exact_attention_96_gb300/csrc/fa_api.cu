@@ -85,11 +85,11 @@ bool encode_bf16_rows(CUtensorMap* m, const void* p, int BH, int N, int d, int r
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// [1, BH, Np] fp32 rows, box (128, 1, 1), no swizzle.
-bool encode_f32_rows(CUtensorMap* m, const void* p, int BH, int Np) {
+// [1, BH, Np] fp32 rows, box (box, 1, 1), no swizzle.
+bool encode_f32_rows(CUtensorMap* m, const void* p, int BH, int Np, int box_len = 128) {
   const cuuint64_t dims[3] = {cuuint64_t(Np), cuuint64_t(BH), 1};
   const cuuint64_t strides[2] = {cuuint64_t(Np) * 4, cuuint64_t(Np) * 4 * BH};
-  const cuuint32_t box[3] = {128, 1, 1};
+  const cuuint32_t box[3] = {cuuint32_t(box_len), 1, 1};
   const cuuint32_t estr[3] = {1, 1, 1};
   return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(p), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
@@ -178,7 +178,6 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
   fa_status st = check_sizes(B, H, N, d);
   if (st != FA_OK) return st;
   if ((st = check_scale(scale)) != FA_OK) return st;
-  if (d == 256) return FA_ERR_UNSUPPORTED;
   const WsLayout w = ws_layout(B, H, N, d);
   if (workspace_bytes < w.total) return FA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dout) ||
@@ -197,6 +196,11 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
       !encode_bf16_rows(&maps.v, v, BH, N, d, 128) || !encode_bf16_rows(&maps.dout, dout, BH, N, d, 128) ||
       !encode_bf16_rows(&m_dk, dk, BH, N, d, 128) || !encode_bf16_rows(&m_dv, dv, BH, N, d, 128) ||
       !encode_f32_rows(&m_lse2, ws + w.lse2_off, BH, w.Np) || !encode_f32_rows(&m_dvec, ws + w.dvec_off, BH, w.Np))
+    return FA_ERR_CUDA;
+  if (d == 256 && (!encode_bf16_rows(&maps.q64, q, BH, N, d, 64) ||
+                   !encode_bf16_rows(&maps.dout64, dout, BH, N, d, 64) ||
+                   !encode_f32_rows(&maps.lse2_64, ws + w.lse2_off, BH, w.Np, 64) ||
+                   !encode_f32_rows(&maps.dvec_64, ws + w.dvec_off, BH, w.Np, 64)))
     return FA_ERR_CUDA;
   fa::BwdArgs a;
   a.q = static_cast<const uint16_t*>(q);

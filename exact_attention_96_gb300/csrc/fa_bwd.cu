@@ -63,8 +63,12 @@ fa_bwd_prep_kernel(const uint16_t* __restrict__ o, const uint16_t* __restrict__ 
   const int bh = int(prow / (n_q_tiles * 128));
   const int i = int(prow % (n_q_tiles * 128));
 
-  // zero this row's part of the dQ accumulator tile: column groups 2*sub, 2*sub+1
-  {
+  // zero this row's part of the dQ accumulator (columns 8*sub .. 8*sub+7)
+  if constexpr (D == 256) {  // row-major [B*H][padded rows][256]
+    float4* row = reinterpret_cast<float4*>(dq_acc + (size_t)prow * D);
+    row[2 * sub] = make_float4(0.f, 0.f, 0.f, 0.f);
+    row[2 * sub + 1] = make_float4(0.f, 0.f, 0.f, 0.f);
+  } else {  // tile order [B*H][q tile][D/4][128][4]: column groups 2*sub, 2*sub+1
     const int qt = i >> 7, t = i & 127;
     float4* tile = reinterpret_cast<float4*>(dq_acc + ((size_t)bh * n_q_tiles + qt) * 128 * D);
     tile[(2 * sub) * 128 + t] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -97,9 +101,26 @@ template <int D>
 __global__ void __launch_bounds__(256)
 fa_bwd_dq_kernel(const float* __restrict__ dq_acc, uint16_t* __restrict__ dq, int N, int n_q_tiles,
                  int BH, float scale) {
-  // thread -> (tile row t = fastest, group of 8 columns k)
   constexpr int kK = D / 8;
   const long long gid = (long long)blockIdx.x * 256 + threadIdx.x;
+  if constexpr (D == 256) {  // row-major accumulator: thread -> (padded row, 8 columns k)
+    const long long prow = gid / kK;
+    const int k = int(gid % kK);
+    if (prow >= (long long)BH * n_q_tiles * 128) return;
+    const int bh = int(prow / (n_q_tiles * 128));
+    const int i = int(prow % (n_q_tiles * 128));
+    if (i >= N) return;
+    const float4* src = reinterpret_cast<const float4*>(dq_acc + (size_t)prow * D) + 2 * k;
+    const float4 a = src[0], b = src[1];
+    uint4 w;
+    w.x = pack_bf16x2(a.x * scale, a.y * scale);
+    w.y = pack_bf16x2(a.z * scale, a.w * scale);
+    w.z = pack_bf16x2(b.x * scale, b.y * scale);
+    w.w = pack_bf16x2(b.z * scale, b.w * scale);
+    *reinterpret_cast<uint4*>(dq + ((size_t)bh * N + i) * D + k * 8) = w;
+    return;
+  }
+  // tile-order accumulator: thread -> (tile row t = fastest, group of 8 columns k)
   const long long per_tile = 128LL * kK;
   const long long total = (long long)BH * n_q_tiles * per_tile;
   if (gid >= total) return;
@@ -560,7 +581,8 @@ cudaError_t launch_prep_and_convert(const BwdArgs& a, int Np, int n_q_tiles, cud
 
 }  // namespace
 
-// Workspace: [D: BH x Np][LSE2: BH x Np][dQ accumulator: BH x n_q_tiles x 128 x d], fp32.
+// Workspace: [D: BH x Np][LSE2: BH x Np][dQ accumulator: BH x n_q_tiles x 128 x d], fp32
+// (tile order for d <= 128, row-major for d = 256).
 cudaError_t launch_bwd_all(const BwdMaps& m, const CUtensorMap& lse2, const CUtensorMap& dmap,
                            const CUtensorMap& dk, const CUtensorMap& dv, const BwdArgs& a, bool causal,
                            int Np, cudaStream_t s) {
@@ -579,6 +601,11 @@ cudaError_t launch_bwd_all(const BwdMaps& m, const CUtensorMap& lse2, const CUte
                  : launch_main<128, 2, false>(m, lse2, dmap, dk, dv, a, s);
       if (e != cudaSuccess) return e;
       return launch_prep_and_convert<128>(a, Np, n_q_tiles, s, false);
+    case 256:
+      if ((e = launch_prep_and_convert<256>(a, Np, n_q_tiles, s, true)) != cudaSuccess) return e;
+      e = launch_bwd_main_d256(m.q64, m.k, m.v, m.dout64, m.lse2_64, m.dvec_64, dk, dv, a, causal, s);
+      if (e != cudaSuccess) return e;
+      return launch_prep_and_convert<256>(a, Np, n_q_tiles, s, false);
     default:
       return cudaErrorInvalidValue;
   }

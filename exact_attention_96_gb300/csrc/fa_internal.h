@@ -55,7 +55,15 @@ struct BwdArgs {
 
 struct BwdMaps {
   CUtensorMap q, k, v, dout;  // 64-column x 128-row boxes
+  // head dim 256 only: Q and dO with 64-row boxes, LSE*log2e and D with 64-entry boxes
+  CUtensorMap q64, dout64, lse2_64, dvec_64;
 };
+
+// Backward main kernel for d = 256 (fa_bwd_d256.cu).
+cudaError_t launch_bwd_main_d256(const CUtensorMap& q64, const CUtensorMap& k, const CUtensorMap& v,
+                                 const CUtensorMap& dout64, const CUtensorMap& lse2_64,
+                                 const CUtensorMap& d64, const CUtensorMap& dk, const CUtensorMap& dv,
+                                 const BwdArgs& a, bool causal, cudaStream_t s);
 
 // Backward: prep, main and dQ-convert launches.  `lse2` and `dvec` describe the fp32
 // [B*H, Np] rows of the workspace (box 128 x 1 x 1); `dk`, `dv` the bf16 outputs.

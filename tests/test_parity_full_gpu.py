@@ -145,3 +145,11 @@ def test_wide_head_d256_fwd(causal):
         assert max_abs(o[b, h, rows], o_ref) <= O_MAX_ABS
         assert rel_fro(o[b, h, rows], o_ref) <= O_REL_FRO
         assert max_abs(lse[b, h, rows], lse_ref) <= LSE_MAX_ABS
+
+
+def test_wide_head_d256_causal_fwd_bwd():
+    # B=2, H=8, N=16384, d=256, causal forward + backward: one whole head against the oracle,
+    # key-sum identities on every head
+    host, o, lse, grads = run(2, 8, 16384, 256, True, seed=80)
+    check_whole_heads(host, o, lse, grads, [(1, 5)], 256, True)
+    check_identities(grads, host[3])

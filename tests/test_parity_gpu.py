@@ -108,6 +108,9 @@ BWD_SMALL = [
     (1, 2, 200, 128, True),
     (2, 1, 640, 128, False),
     (1, 1, 513, 128, True),
+    (1, 1, 64, 256, False),
+    (1, 2, 200, 256, False),
+    (2, 1, 333, 256, True),
 ]
 
 
