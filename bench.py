@@ -264,6 +264,103 @@ def run_gpu(args, rank, world, local_rank):
                 clocks=clocks.summary())
 
 
+# ------------------------------------------------------------------- sweep ----
+
+SWEEP = [  # (name, B, H, N, d, causal, multiplier, passes)
+    ("pr1", 1, 1, 128, 64, False, 1.0, ("fwd",)),
+    ("gpt2-medium", 64, 16, 1024, 64, False, 1.0, ("fwd", "bwd")),
+    ("mem-1k", 16, 8, 1024, 64, False, 1.0, ("fwd", "bwd")),
+    ("mem-2k", 16, 8, 2048, 64, False, 1.0, ("fwd", "bwd")),
+    ("mem-4k", 16, 8, 4096, 64, False, 1.0, ("fwd", "bwd")),
+    ("long-causal", 4, 16, 8192, 128, True, 0.5, ("fwd", "bwd")),
+    ("long-seq-nc", 1, 8, 65536, 64, False, 1.0, ("fwd",)),
+    ("long-seq-c", 1, 8, 65536, 64, True, 1.0, ("fwd", "bwd")),
+    ("wide-head-nc", 2, 8, 16384, 256, False, 1.0, ("fwd",)),
+    ("wide-head-c", 2, 8, 16384, 256, True, 1.0, ("fwd", "bwd")),
+]
+
+
+def naive_peak_bytes(q, k, v, do, scale):
+    """Peak extra device memory of standard attention in PyTorch eager (S and P materialised
+    in HBM, backward through autograd) -- the comparison the memory experiment makes."""
+    import torch
+    torch.cuda.synchronize()
+    torch.cuda.reset_peak_memory_stats()
+    base = torch.cuda.memory_allocated()
+    qq, kk, vv = (t.detach().clone().requires_grad_(True) for t in (q, k, v))
+    s = torch.matmul(qq, kk.transpose(-1, -2)) * scale
+    p = torch.softmax(s.float(), dim=-1).to(q.dtype)
+    o = torch.matmul(p, vv)
+    o.backward(do)
+    torch.cuda.synchronize()
+    peak = torch.cuda.max_memory_allocated() - base
+    del qq, kk, vv, s, p, o
+    return peak
+
+
+def run_sweep(reps: int = 20):
+    import numpy as np
+    import torch
+    from exact_attention_96_gb300 import abi, build, inputs as I
+    from exact_attention_96_gb300 import attention as fa
+
+    build.build()
+    abi.load()
+    peaks, src = load_peaks()
+    burst, sustained = peaks["bf16_tflops"], peaks.get("bf16_tflops_sustained") or peaks["bf16_tflops"]
+    for name, B, H, N, d, causal, mult, passes in SWEEP:
+        host = I.attention_inputs(B, H, N, d, seed=7, multiplier=mult)
+        q, k, v, do = (torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).cuda() for x in host)
+        scale = 1 / math.sqrt(d)
+        fwd_f, bwd_f = step_flops(B, H, N, d, causal)
+        o, lse = fa.forward(q, k, v, causal=causal, scale=scale)
+        ws = torch.empty(fa.workspace_bytes(B, H, N, d), dtype=torch.uint8, device="cuda")
+        grads = tuple(torch.empty_like(q) for _ in range(3))
+        calls = {"fwd": lambda: fa.forward(q, k, v, causal=causal, scale=scale, out=o, lse=lse),
+                 "bwd": lambda: fa.backward(q, k, v, o, do, lse, causal=causal, scale=scale,
+                                            workspace=ws, grads=grads)}
+        for ps in passes:
+            for _ in range(3):
+                calls[ps]()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(reps):
+                calls[ps]()
+            e1.record()
+            torch.cuda.synchronize()
+            ms = e0.elapsed_time(e1) / reps
+            flops = fwd_f if ps == "fwd" else bwd_f
+            tf = flops / (ms * 1e-3) / 1e12
+            line = {"config": name, "shape": [B, H, N, d], "causal": causal, "pass": ps, "ms": ms,
+                    "tflops": tf, "frac_sustained": tf / sustained, "frac_burst": tf / burst,
+                    "peak_source": src}
+            if ps == "fwd":
+                line["alg_gbs"] = (8.0 * B * H * N * d + 4.0 * B * H * N) / (ms * 1e-3) / 1e9
+            print(json.dumps(line), flush=True)
+        if fa.status_check() != abi.FA_OK:
+            raise RuntimeError(f"device status not OK after {name}")
+        if name.startswith("mem-"):
+            torch.cuda.synchronize()
+            torch.cuda.reset_peak_memory_stats()
+            base = torch.cuda.memory_allocated()
+            del o, lse, ws, grads, calls
+            torch.cuda.synchronize()
+            base = torch.cuda.memory_allocated()
+            torch.cuda.reset_peak_memory_stats()
+            o2, l2 = fa.forward(q, k, v, causal=causal, scale=scale)
+            g2 = fa.backward(q, k, v, o2, do, l2, causal=causal, scale=scale)
+            torch.cuda.synchronize()
+            ours = torch.cuda.max_memory_allocated() - base
+            del o2, l2, g2
+            naive = naive_peak_bytes(q, k, v, do, scale)
+            print(json.dumps({"config": name, "peak_extra_MB_fa": ours / 2**20,
+                              "peak_extra_MB_naive_eager": naive / 2**20,
+                              "note": "extra device memory beyond q, k, v, dO for one fwd+bwd"}), flush=True)
+        del q, k, v, do
+        torch.cuda.empty_cache()
+
+
 # -------------------------------------------------------------------- main ----
 
 def kernel_traffic(kernel_file: str):
@@ -295,7 +392,12 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sweep", action="store_true",
+                    help="time every workload shape (one JSON line per shape and pass) and exit")
     args = ap.parse_args()
+    if args.sweep:
+        run_sweep()
+        return
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
 
