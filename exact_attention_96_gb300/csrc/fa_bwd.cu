@@ -403,10 +403,11 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
       // phase 1: P^T
       if (!__all_sync(0xffffffffu, mbar_wait(bar(L::kBarSFull), ph, wc))) { ok = false; break; }
       tc_fence_after_sync();
+      uint32_t rs[64];
+      tmem_ld64(tmem + lane_off + L::kColS + c0, rs);  // this half's 64 S^T columns, one wait
 #pragma unroll
       for (int cc = 0; cc < 64; cc += 32) {
-        uint32_t r[32];
-        tmem_ld32(tmem + lane_off + L::kColS + c0 + cc, r);
+        const uint32_t* r = rs + cc;
         float lv[32];
 #pragma unroll
         for (int e = 0; e < 32; e += 4) {
@@ -439,8 +440,7 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
       for (int cc = 0; cc < 64; cc += 32) {
         uint32_t r[32];
         uint32_t pr[16];
-        tmem_ld32(tmem + lane_off + L::kColDP + c0 + cc, r);
-        tmem_ld16(tmem + lane_off + L::kColS + c0 + cc / 2, pr);
+        tmem_ld32_ld16(tmem + lane_off + L::kColDP + c0 + cc, r, tmem + lane_off + L::kColS + c0 + cc / 2, pr);
         float dl[32];
 #pragma unroll
         for (int e = 0; e < 32; e += 4) {

@@ -246,12 +246,12 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       if (!__all_sync(0xffffffffu, mbar_wait(bar(L::kBarSFull + b), (j >> 1) & 1, wc))) { ok = false; break; }
       tc_fence_after_sync();
       float s[BC];
+      {  // the whole S row in one TMEM load (one wait)
+        uint32_t r[BC];
+        if constexpr (BC == 128) tmem_ld128(tmem + lane_off + L::kColS + b * BC, r);
+        else tmem_ld64(tmem + lane_off + L::kColS + b * BC, r);
 #pragma unroll
-      for (int c = 0; c < BC; c += 32) {
-        uint32_t r[32];
-        tmem_ld32(tmem + lane_off + L::kColS + b * BC + c, r);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) s[c + i] = __uint_as_float(r[i]);
+        for (int i = 0; i < BC; ++i) s[i] = __uint_as_float(r[i]);
       }
       tc_fence_before_sync();
       mbar_arrive(bar(L::kBarSFree + b));
