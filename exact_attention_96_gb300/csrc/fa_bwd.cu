@@ -345,13 +345,14 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                  (it > 0 || kk > 0) ? 1u : 0u);
         }
         mma_commit(bar(L::kBarDVDone));
-        if (!mbar_wait(bar(L::kBarDSReady), ph, wc)) { ok = false; break; }
-        // S_{i+1} overwrites P^T_i: the dV product reading it must have completed, and the
-        // key-row warps have finished reading it (they published dS_i after that).
+        // S_{i+1} overwrites P^T_i, whose only reader is the dV product (the key-row warps
+        // keep their own copy of P in registers): issue it as soon as dV_i has completed, so
+        // the tensor core runs dV_i and S_{i+1} while the key rows compute dS_i.
         if (it + 1 < n_it && !(mbar_wait(bar(L::kBarDVDone), ph, wc) && issue_s(it + 1))) {
           ok = false;
           break;
         }
+        if (!mbar_wait(bar(L::kBarDSReady), ph, wc)) { ok = false; break; }
         tc_fence_after_sync();
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk) {
@@ -405,6 +406,7 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
       tc_fence_after_sync();
       uint32_t rs[64];
       tmem_ld64(tmem + lane_off + L::kColS + c0, rs);  // this half's 64 S^T columns, one wait
+      uint32_t pkeep[32];  // P^T of this half (bf16 pairs), kept for phase 2
 #pragma unroll
       for (int cc = 0; cc < 64; cc += 32) {
         const uint32_t* r = rs + cc;
@@ -426,6 +428,8 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
           }
           w[e / 2] = pack_bf16x2(p0, p1);
         }
+#pragma unroll
+        for (int e = 0; e < 16; ++e) pkeep[cc / 2 + e] = w[e];
         tmem_st16(tmem + lane_off + L::kColS + c0 + cc / 2, w);
       }
       tmem_wait_st();
@@ -439,8 +443,8 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
 #pragma unroll
       for (int cc = 0; cc < 64; cc += 32) {
         uint32_t r[32];
-        uint32_t pr[16];
-        tmem_ld32_ld16(tmem + lane_off + L::kColDP + c0 + cc, r, tmem + lane_off + L::kColS + c0 + cc / 2, pr);
+        tmem_ld32(tmem + lane_off + L::kColDP + c0 + cc, r);
+        const uint32_t* pr = pkeep + cc / 2;
         float dl[32];
 #pragma unroll
         for (int e = 0; e < 32; e += 4) {
