@@ -38,6 +38,7 @@ SIGNATURES = {
     "fa_status_check": (_c_int, [_c_void_p]),
     "fa_status_string": (ctypes.c_char_p, [_c_int]),
     "fa_set_wait_limit_ns": (ctypes.c_uint64, [ctypes.c_uint64]),
+    "fa_test_withhold_kv_tile": (_c_int, [_c_int]),
 }
 
 _lib = None
@@ -98,3 +99,7 @@ def fa_status_check(stream) -> int:
 
 def fa_set_wait_limit_ns(ns: int) -> int:
     return load().fa_set_wait_limit_ns(ns)
+
+
+def fa_test_withhold_kv_tile(tile: int) -> int:
+    return load().fa_test_withhold_kv_tile(tile)

@@ -23,6 +23,7 @@ std::mutex g_mu;
 int* g_err_ptr[kMaxDevices] = {};
 int g_cc_ok[kMaxDevices] = {};  // 0 unknown, 1 sm_103, -1 other
 std::atomic<uint64_t> g_wait_limit_ns{2000000000ull};
+std::atomic<int> g_withhold_k_tile{-1};  // one-shot test hook for the next fa_fwd launch
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
 fa_status cuda_fail(cudaError_t) { return FA_ERR_CUDA; }
@@ -131,6 +132,8 @@ const char* fa_status_string(fa_status s) {
   return "FA_ERR_UNKNOWN";
 }
 
+int fa_test_withhold_kv_tile(int tile) { return g_withhold_k_tile.exchange(tile < 0 ? -1 : tile); }
+
 uint64_t fa_set_wait_limit_ns(uint64_t ns) {
   if (ns < 1000000ull) ns = 1000000ull;
   return g_wait_limit_ns.exchange(ns);
@@ -162,6 +165,7 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
   a.scale_log2 = scale * 1.4426950408889634f;
   a.wait_limit_ns = g_wait_limit_ns.load();
   a.err_word = err;
+  a.withhold_k_tile = g_withhold_k_tile.exchange(-1);
   const cudaError_t e = fa::launch_fwd(maps, a, d, causal != 0, reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FA_OK : cuda_fail(e);
 }

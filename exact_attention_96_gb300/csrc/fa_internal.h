@@ -18,6 +18,7 @@ struct FwdArgs {
   float scale_log2;     // scale * log2(e)
   uint64_t wait_limit_ns;
   int* err_word;        // per-device error word
+  int withhold_k_tile;  // test hook: the producer never loads this K tile (-1: none)
 };
 
 // Tensor maps of one [B*H, N, d] bf16 tensor: `rows128` boxes of 64 columns x 128 rows,

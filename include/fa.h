@@ -129,6 +129,16 @@ const char* fa_status_string(fa_status s);
  */
 uint64_t fa_set_wait_limit_ns(uint64_t ns);
 
+/*
+ * Test hook for the failure path (not needed in normal use).  The next fa_fwd launch, on any
+ * device, withholds the load of key/value tile `tile` (tile t = keys [t*Bc, (t+1)*Bc)):
+ * its barrier is never armed, so the waits that depend on it give up after the wait limit,
+ * the kernel records FA_ERR_TIMEOUT in the device's error word, releases its resources and
+ * exits with O and LSE unspecified; the device context stays usable.  One-shot: the launch
+ * consumes the request.  tile < 0 cancels a pending request.  Returns the previous request.
+ */
+int fa_test_withhold_kv_tile(int tile);
+
 #ifdef __cplusplus
 }
 #endif

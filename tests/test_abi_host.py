@@ -108,3 +108,9 @@ def test_wait_limit_round_trip(lib):
     prev = abi.fa_set_wait_limit_ns(5_000_000_000)
     assert abi.fa_set_wait_limit_ns(10) == 5_000_000_000  # raised to the 1 ms floor on store
     assert abi.fa_set_wait_limit_ns(prev) == 1_000_000
+
+
+def test_withhold_hook_is_one_shot_request(lib):
+    assert abi.fa_test_withhold_kv_tile(3) == -1
+    assert abi.fa_test_withhold_kv_tile(-5) == 3   # cancel
+    assert abi.fa_test_withhold_kv_tile(-1) == -1
