@@ -380,12 +380,13 @@ cudaError_t launch_cfg(const Maps& m, const FwdArgs& a, cudaStream_t s) {
 
 }  // namespace
 
-int fwd_kv_tile(int d) { return d == 256 ? 64 : 128; }
+int fwd_kv_tile(int d) { return d == 128 ? 128 : 64; }
 
 cudaError_t launch_fwd(const Maps& m, const FwdArgs& a, int d, bool causal, cudaStream_t s) {
   switch (d) {
     case 64:
-      return causal ? launch_cfg<64, 128, 4, true>(m, a, s) : launch_cfg<64, 128, 4, false>(m, a, s);
+      // 64-key tiles keep TMEM at 256 columns and shared memory near 81 KB: two CTAs per SM
+      return causal ? launch_cfg<64, 64, 4, true>(m, a, s) : launch_cfg<64, 64, 4, false>(m, a, s);
     case 128:
       return causal ? launch_cfg<128, 128, 2, true>(m, a, s) : launch_cfg<128, 128, 2, false>(m, a, s);
     case 256:
