@@ -27,6 +27,11 @@ _c_size_t = ctypes.c_size_t
 SIGNATURES = {
     "fa_fwd": (_c_int, [_c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_void_p,
                         _c_int, _c_int, _c_int, _c_int, _c_float, _c_int, _c_void_p]),
+    "fa_fwd_splitkv_workspace_bytes": (_c_size_t, [_c_int] * 6),
+    "fa_fwd_splitkv_num_splits": (_c_int, [_c_int] * 6),
+    "fa_fwd_splitkv": (_c_int, [_c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_void_p,
+                                _c_int, _c_int, _c_int, _c_int, _c_int, _c_float, _c_int,
+                                _c_void_p, _c_size_t, _c_void_p]),
     "fa_bwd_workspace_bytes": (_c_size_t, [_c_int, _c_int, _c_int, _c_int]),
     "fa_bwd": (_c_int, [_c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_void_p,
                         _c_void_p, _c_void_p, _c_void_p,
@@ -78,6 +83,18 @@ def check(fn: str, status: int) -> None:
 
 def fa_fwd(q, k, v, o, lse, B, H, N, d, scale, causal, stream) -> int:
     return load().fa_fwd(q, k, v, o, lse, B, H, N, d, scale, int(causal), stream)
+
+
+def fa_fwd_splitkv_workspace_bytes(B, H, Nq, Nk, d, num_splits) -> int:
+    return load().fa_fwd_splitkv_workspace_bytes(B, H, Nq, Nk, d, num_splits)
+
+
+def fa_fwd_splitkv_num_splits(B, H, Nq, Nk, d, num_splits) -> int:
+    return load().fa_fwd_splitkv_num_splits(B, H, Nq, Nk, d, num_splits)
+
+
+def fa_fwd_splitkv(q, k, v, o, lse, B, H, Nq, Nk, d, scale, num_splits, ws, ws_bytes, stream) -> int:
+    return load().fa_fwd_splitkv(q, k, v, o, lse, B, H, Nq, Nk, d, scale, num_splits, ws, ws_bytes, stream)
 
 
 def fa_bwd_workspace_bytes(B, H, N, d) -> int:

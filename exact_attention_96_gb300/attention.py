@@ -41,6 +41,30 @@ def forward(q, k, v, causal: bool = False, scale: float | None = None, out=None,
     return o, l
 
 
+def forward_splitkv(q, k, v, num_splits: int = 0, scale: float | None = None, out=None, lse=None,
+                    workspace=None):
+    """Split-KV forward (no mask): q [B,H,Nq,d] against k, v [B,H,Nk,d]; returns (O, LSE)."""
+    for t in (q, k, v):
+        if not t.is_cuda or t.dtype != torch.bfloat16 or not t.is_contiguous() or t.dim() != 4:
+            raise ValueError("expected contiguous bf16 CUDA tensors [B, H, N, d]")
+    B, H, Nq, d = q.shape
+    Nk = k.shape[2]
+    if k.shape != (B, H, Nk, d) or v.shape != k.shape:
+        raise ValueError("k and v must be [B, H, Nk, d] with q's B, H, d")
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    o = torch.empty_like(q) if out is None else out
+    l = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device) if lse is None else lse
+    nbytes = abi.fa_fwd_splitkv_workspace_bytes(B, H, Nq, Nk, d, num_splits)
+    if workspace is None:
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+    with torch.cuda.device(q.device):
+        st = abi.fa_fwd_splitkv(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), l.data_ptr(),
+                                B, H, Nq, Nk, d, scale, num_splits, workspace.data_ptr(),
+                                workspace.numel(), _stream(q))
+    abi.check("fa_fwd_splitkv", st)
+    return o, l
+
+
 def workspace_bytes(B: int, H: int, N: int, d: int) -> int:
     return abi.fa_bwd_workspace_bytes(B, H, N, d)
 

@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstdint>
@@ -160,6 +161,11 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
   fa::FwdArgs a;
   a.lse = lse;
   a.N = N;
+  a.Nk = N;
+  a.num_splits = 1;
+  a.tiles_per_split = (N + kv_rows - 1) / kv_rows;
+  a.o_part = nullptr;
+  a.lse_part = nullptr;
   a.BH = BH;
   a.n_q_tiles = (N + 127) / 128;
   a.scale_log2 = scale * 1.4426950408889634f;
@@ -167,6 +173,89 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
   a.err_word = err;
   a.withhold_k_tile = g_withhold_k_tile.exchange(-1);
   const cudaError_t e = fa::launch_fwd(maps, a, d, causal != 0, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : cuda_fail(e);
+}
+
+namespace {
+
+struct SplitPlan {
+  int splits, tiles_per_split;
+  size_t lse_off, total;
+};
+
+// Key-range split: `requested` <= 0 picks enough splits for about two CTAs per SM of a
+// 152-SM part (independent of the device, so the workspace size is a pure function of the
+// sizes); every split gets at least one key tile.
+SplitPlan split_plan(int B, int H, int Nq, int Nk, int d, int requested) {
+  SplitPlan p{};
+  const int bc = fa::fwd_kv_tile(d);
+  const int n_tiles = (Nk + bc - 1) / bc;
+  const long long base = (long long)((Nq + 127) / 128) * B * H;
+  int want = requested > 0 ? requested : int(std::min<long long>(256, (304 + base - 1) / base));
+  want = std::max(1, std::min(want, n_tiles));
+  p.tiles_per_split = (n_tiles + want - 1) / want;
+  p.splits = (n_tiles + p.tiles_per_split - 1) / p.tiles_per_split;
+  const size_t rows = size_t(B) * H * Nq;
+  p.lse_off = round256(size_t(p.splits) * rows * d * 4);
+  p.total = p.lse_off + size_t(p.splits) * rows * 4;
+  return p;
+}
+
+}  // namespace
+
+size_t fa_fwd_splitkv_workspace_bytes(int B, int H, int Nq, int Nk, int d, int num_splits) {
+  if (check_sizes(B, H, Nq, d) != FA_OK || check_sizes(B, H, Nk, d) != FA_OK || num_splits > 1024) return 0;
+  return split_plan(B, H, Nq, Nk, d, num_splits).total;
+}
+
+int fa_fwd_splitkv_num_splits(int B, int H, int Nq, int Nk, int d, int num_splits) {
+  if (check_sizes(B, H, Nq, d) != FA_OK || check_sizes(B, H, Nk, d) != FA_OK || num_splits > 1024) return 0;
+  return split_plan(B, H, Nq, Nk, d, num_splits).splits;
+}
+
+fa_status fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                         int Nq, int Nk, int d, float scale, int num_splits, void* workspace,
+                         size_t workspace_bytes, fa_stream_t stream) {
+  if (!q || !k || !v || !o || !lse || !workspace) return FA_ERR_INVALID_ARG;
+  fa_status st = check_sizes(B, H, Nq, d);
+  if (st != FA_OK) return st;
+  if ((st = check_sizes(B, H, Nk, d)) != FA_OK) return st;
+  if ((st = check_scale(scale)) != FA_OK) return st;
+  if (num_splits > 1024) return FA_ERR_UNSUPPORTED;
+  const SplitPlan plan = split_plan(B, H, Nq, Nk, d, num_splits);
+  if (workspace_bytes < plan.total) return FA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return FA_ERR_MISALIGNED;
+  int dev = 0;
+  int* err = nullptr;
+  if ((st = device_setup(&dev, &err)) != FA_OK) return st;
+  const int BH = B * H;
+  const int kv_rows = fa::fwd_kv_tile(d);
+  fa::Maps maps;
+  if (!encode_bf16_rows(&maps.q, q, BH, Nq, d, 128) || !encode_bf16_rows(&maps.k, k, BH, Nk, d, kv_rows) ||
+      !encode_bf16_rows(&maps.v, v, BH, Nk, d, kv_rows) || !encode_bf16_rows(&maps.o, o, BH, Nq, d, 128))
+    return FA_ERR_CUDA;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  fa::FwdArgs a;
+  a.lse = lse;
+  a.N = Nq;
+  a.Nk = Nk;
+  a.num_splits = plan.splits;
+  a.tiles_per_split = plan.tiles_per_split;
+  a.o_part = reinterpret_cast<float*>(ws);
+  a.lse_part = reinterpret_cast<float*>(ws + plan.lse_off);
+  a.BH = BH;
+  a.n_q_tiles = (Nq + 127) / 128;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.wait_limit_ns = g_wait_limit_ns.load();
+  a.err_word = err;
+  a.withhold_k_tile = -1;
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = fa::launch_fwd(maps, a, d, false, s);
+  if (e != cudaSuccess) return cuda_fail(e);
+  e = fa::launch_splitkv_combine(a.o_part, a.lse_part, static_cast<uint16_t*>(o), lse,
+                                 (long long)BH * Nq, plan.splits, d, s);
   return e == cudaSuccess ? FA_OK : cuda_fail(e);
 }
 

@@ -94,9 +94,13 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
   const int bh = blockIdx.y;
   const int q_tile = CAUSAL ? (args.n_q_tiles - 1 - int(blockIdx.x)) : int(blockIdx.x);
   const int q0 = q_tile * kBM;
-  const int N = args.N;
-  const int n_kv_all = (N + BC - 1) / BC;
-  const int nkv = CAUSAL ? min(n_kv_all, (q0 + kBM + BC - 1) / BC) : n_kv_all;
+  const int N = args.N;    // query rows
+  const int Nk = args.Nk;  // keys
+  const int n_kv_all = (Nk + BC - 1) / BC;
+  // this CTA's key tiles: [t_begin, t_begin + nkv) (split mode: one range per blockIdx.z)
+  const int t_begin = int(blockIdx.z) * args.tiles_per_split;
+  const int nkv = CAUSAL ? min(n_kv_all, (q0 + kBM + BC - 1) / BC)
+                         : min(n_kv_all - t_begin, args.tiles_per_split);
 
   auto bar = [&](int i) -> uint32_t { return base + L::kBarOff + 8u * uint32_t(i); };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
@@ -157,13 +161,13 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         if (j != args.withhold_k_tile) {  // the test hook leaves this tile's barrier unarmed
           mbar_arrive_expect_tx(bar(L::kBarKFull + st), L::kKVBytes);
           for (int s = 0; s < L::kSlabs; ++s)
-            tma_load_3d(sK(st) + s * (BC * 128), &tmK, bar(L::kBarKFull + st), s * 64, j * BC, bh);
+            tma_load_3d(sK(st) + s * (BC * 128), &tmK, bar(L::kBarKFull + st), s * 64, (t_begin + j) * BC, bh);
           ++k_arms[st];
         }
         if (j >= NS && !mbar_wait(bar(L::kBarVEmpty + st), ph ^ 1, wc)) { ok = false; break; }
         mbar_arrive_expect_tx(bar(L::kBarVFull + st), L::kKVBytes);
         for (int s = 0; s < L::kSlabs; ++s)
-          tma_load_3d(sV(st) + s * (BC * 128), &tmV, bar(L::kBarVFull + st), s * 64, j * BC, bh);
+          tma_load_3d(sV(st) + s * (BC * 128), &tmV, bar(L::kBarVFull + st), s * 64, (t_begin + j) * BC, bh);
         ++v_arms[st];
       }
       if (!ok) {
@@ -259,8 +263,8 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       mbar_arrive(bar(L::kBarSFree + b));
 
       // keys kv0 + c are visible for c < lim (sequence tail; causal: key <= query)
-      const int kv0 = j * BC;
-      int lim = N - kv0;
+      const int kv0 = (t_begin + j) * BC;
+      int lim = Nk - kv0;
       if (CAUSAL) lim = min(lim, row_g - kv0 + 1);
       if (lim < BC) {
 #pragma unroll
@@ -324,7 +328,26 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
 
     // ------------------------------------------------------------ epilogue ----
     const bool fin = ok && __all_sync(0xffffffffu, mbar_wait(bar(L::kBarOFinal), 0, wc));
-    if (fin) {
+    const bool split_mode = args.o_part != nullptr;
+    if (fin && split_mode) {
+      // partial output of this key range: O normalised by its own l (fp32) and its LSE
+      tc_fence_after_sync();
+      const float inv_l = 1.f / l_run;
+      const size_t prow = (size_t(blockIdx.z) * args.BH + bh) * N + row_g;
+#pragma unroll 1
+      for (int c = 0; c < D; c += 32) {
+        uint32_t r[32];
+        tmem_ld32(tmem + lane_off + L::kColO + c, r);
+        if (row_g < N) {
+          float4* dst = reinterpret_cast<float4*>(args.o_part + prow * D + c);
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            dst[i] = make_float4(__uint_as_float(r[4 * i]) * inv_l, __uint_as_float(r[4 * i + 1]) * inv_l,
+                                 __uint_as_float(r[4 * i + 2]) * inv_l, __uint_as_float(r[4 * i + 3]) * inv_l);
+        }
+      }
+      if (row_g < N) args.lse_part[prow] = (m_run + lg2_approx(l_run)) * 0.69314718055994531f;
+    } else if (fin) {
       tc_fence_after_sync();
       const float inv_l = 1.f / l_run;
       uint8_t* stage = smem + L::kQOff;  // Q is no longer read by any MMA
@@ -352,7 +375,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     // Every softmax thread arrives (finished or not); thread 0 stores the tile only when all
     // 128 rows were staged and no wait in the CTA gave up.
     mbar_arrive(bar(L::kBarEpi));
-    if (threadIdx.x == 0 && fin && mbar_wait(bar(L::kBarEpi), 0, wc) && *abort_flag == 0) {
+    if (threadIdx.x == 0 && fin && !split_mode && mbar_wait(bar(L::kBarEpi), 0, wc) && *abort_flag == 0) {
       for (int s = 0; s < L::kSlabs; ++s) tma_store_3d(&tmO, sQ + s * (kBM * 128), s * 64, q0, bh);
       bulk_commit_group();
       bulk_wait_group_all();
@@ -373,7 +396,7 @@ cudaError_t launch_cfg(const Maps& m, const FwdArgs& a, cudaStream_t s) {
   auto kern = fa_fwd_kernel<D, BC, NS, CAUSAL>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemAlloc);
   if (e != cudaSuccess) return e;
-  dim3 grid(a.n_q_tiles, a.BH);
+  dim3 grid(a.n_q_tiles, a.BH, a.num_splits);
   kern<<<grid, kThreads, L::kSmemAlloc, s>>>(m.q, m.k, m.v, m.o, a);
   return cudaGetLastError();
 }

@@ -12,7 +12,12 @@ namespace fa {
 // Everything a forward launch needs besides the four tensor maps.
 struct FwdArgs {
   float* lse;           // [B*H, N] fp32
-  int N;                // sequence length
+  int N;                // query rows per head
+  int Nk;               // keys per head (== N for the square problem)
+  int num_splits;       // key-range splits (grid.z); 1 for the square problem
+  int tiles_per_split;  // key tiles per split
+  float* o_part;        // split mode: fp32 [splits][B*H][N][d] partial outputs, else null
+  float* lse_part;      // split mode: fp32 [splits][B*H][N] partial log-sum-exps
   int BH;               // B*H
   int n_q_tiles;        // ceil(N / 128)
   float scale_log2;     // scale * log2(e)
@@ -31,6 +36,11 @@ struct Maps {
 cudaError_t launch_fwd(const Maps& maps, const FwdArgs& a, int d, bool causal, cudaStream_t s);
 // Key-tile height the forward kernel uses for head dim d (the K/V tensor-map box height).
 int fwd_kv_tile(int d);
+
+// Split-KV merge: o [rows, d] bf16 and lse [rows] from `splits` partial (o, lse) pairs,
+// rows = B*H*Nq.
+cudaError_t launch_splitkv_combine(const float* o_part, const float* lse_part, uint16_t* o, float* lse,
+                                   long long rows, int splits, int d, cudaStream_t s);
 
 struct BwdArgs {
   const uint16_t* q;

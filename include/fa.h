@@ -62,6 +62,25 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
                  int B, int H, int N, int d, float scale, int causal, fa_stream_t stream);
 
 /*
+ * Split-KV forward ("Flash Attention 原理与实践" §5.1, the decoding variant): queries attend to
+ * a key/value sequence of a different length, split into key ranges processed by separate
+ * CTAs; each range writes its partial output (normalised within the range) and partial
+ * log-sum-exp to the workspace, and a merge kernel combines them with log-sum-exp weights
+ * (the re-basing of "FlashAttention 与显存" §08).  No causal mask (every query sees all Nk
+ * keys), which is the decoding case.
+ *   q: bf16 [B,H,Nq,d]; k, v: bf16 [B,H,Nk,d]; o: bf16 [B,H,Nq,d]; lse: fp32 [B,H,Nq].
+ *   num_splits: requested number of key ranges (<= 1024); <= 0 picks one (about two CTAs per
+ *   SM); the effective count (every range non-empty) is fa_fwd_splitkv_num_splits().
+ *   workspace: caller-owned, 256-byte aligned, >= fa_fwd_splitkv_workspace_bytes() bytes.
+ * Errors as for fa_fwd; workspace too small -> FA_ERR_INVALID_ARG.
+ */
+size_t fa_fwd_splitkv_workspace_bytes(int B, int H, int Nq, int Nk, int d, int num_splits);
+int fa_fwd_splitkv_num_splits(int B, int H, int Nq, int Nk, int d, int num_splits);
+fa_status fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse,
+                         int B, int H, int Nq, int Nk, int d, float scale, int num_splits,
+                         void* workspace, size_t workspace_bytes, fa_stream_t stream);
+
+/*
  * Bytes of device workspace fa_bwd needs: D [B,H,N] fp32 followed (at a 256-byte aligned
  * offset) by the fp32 dQ accumulator [B,H,N,d].  Returns 0 for invalid sizes.
  */

@@ -42,6 +42,7 @@ __all__ = [
     "attention_bwd_head",
     "attention_bwd_rows",
     "attention_bwd_key_columns",
+    "lse_merge",
 ]
 
 
@@ -207,3 +208,19 @@ def attention_bwd_key_columns(q_head, k_head, v_head, do_head, scale: float, cau
         dv += p_sel.T @ do[r0:r1]
         dk += scale * (ds_sel.T @ q[r0:r1])
     return dk, dv
+
+
+def lse_merge(o_parts, lse_parts):
+    """Merge attention computed over disjoint key ranges ("Flash Attention 原理与实践" §5.1:
+    split the keys across workers, then combine with log-sum-exp).
+
+    o_parts: [S, ..., d] outputs, each normalised within its own key range; lse_parts:
+    [S, ...] the ranges' log-sum-exps.  Returns (O, LSE) of the whole key set:
+    LSE = log sum_s exp(LSE_s),  O = sum_s exp(LSE_s - LSE) O_s.
+    """
+    o_parts = np.asarray(o_parts, np.float64)
+    lse_parts = np.asarray(lse_parts, np.float64)
+    m = lse_parts.max(axis=0)
+    lse = m + np.log(np.exp(lse_parts - m).sum(axis=0))
+    w = np.exp(lse_parts - lse)
+    return (w[..., None] * o_parts).sum(axis=0), lse

@@ -114,3 +114,18 @@ def test_withhold_hook_is_one_shot_request(lib):
     assert abi.fa_test_withhold_kv_tile(3) == -1
     assert abi.fa_test_withhold_kv_tile(-5) == 3   # cancel
     assert abi.fa_test_withhold_kv_tile(-1) == -1
+
+
+def test_split_plan(lib):
+    # every range non-empty; auto picks about two CTAs per SM for decode shapes
+    n = abi.fa_fwd_splitkv_num_splits
+    assert n(1, 1, 1, 1000, 64, 0) == 16            # 16 tiles of 64 keys, all used
+    assert n(4, 16, 1, 65536, 128, 0) == 5          # 64 CTAs per split -> ceil(304/64)
+    assert n(1, 1, 1, 500, 128, 7) == 4             # 4 tiles: 7 requested, 4 effective
+    assert n(1, 1, 1, 500, 128, 3) == 2             # 2 tiles per range -> 2 ranges
+    assert n(1, 1, 1, 10, 64, 0) == 1
+    assert abi.fa_fwd_splitkv_workspace_bytes(1, 1, 0, 10, 64, 0) == 0
+    assert abi.fa_fwd_splitkv_workspace_bytes(1, 1, 1, 10, 48, 0) == 0
+    ws = abi.fa_fwd_splitkv_workspace_bytes(2, 3, 5, 1000, 64, 4)
+    rows = 2 * 3 * 5
+    assert ws == (4 * rows * 64 * 4 + 255) // 256 * 256 + 4 * rows * 4

@@ -163,6 +163,35 @@ def test_gradient_sums_over_keys():
         assert np.max(np.abs(dk.sum(axis=0))) < 1e-12
 
 
+def test_queries_and_keys_of_different_lengths_match_torch():
+    # the decoding shape: few queries against a long key sequence (no mask)
+    q, k, v = rnd((2, 3, 5, 8), 91), rnd((2, 3, 37, 8), 92), rnd((2, 3, 37, 8), 93)
+    o, lse = A.attention_fwd(q, k, v, 0.4, False)
+    tq, tk, tv = (torch.tensor(x) for x in (q, k, v))
+    ref = F.scaled_dot_product_attention(tq, tk, tv, scale=0.4).numpy()
+    tlse = torch.logsumexp(0.4 * tq @ tk.transpose(-1, -2), dim=-1).numpy()
+    assert np.max(np.abs(o - ref)) < 1e-12
+    assert np.max(np.abs(lse - tlse)) < 1e-12
+
+
+@pytest.mark.parametrize("cuts", [[0, 37], [0, 1, 37], [0, 10, 11, 30, 37], list(range(38))])
+def test_split_key_ranges_merge_to_whole(cuts):
+    q, k, v = rnd((1, 2, 6, 4), 94), rnd((1, 2, 37, 4), 95), rnd((1, 2, 37, 4), 96)
+    o, lse = A.attention_fwd(q, k, v, 0.7, False)
+    parts = [A.attention_fwd(q, k[:, :, a:b], v[:, :, a:b], 0.7, False) for a, b in zip(cuts, cuts[1:])]
+    o_m, lse_m = A.lse_merge([p[0] for p in parts], [p[1] for p in parts])
+    assert np.max(np.abs(o_m - o)) < 1e-12
+    assert np.max(np.abs(lse_m - lse)) < 1e-12
+
+
+def test_merge_is_not_a_plain_average():
+    # planted slip: averaging the parts (dropping the exp(LSE_s - LSE) weights) must differ
+    q, k, v = rnd((1, 1, 4, 4), 97), rnd((1, 1, 20, 4), 98), rnd((1, 1, 20, 4), 99)
+    o, _ = A.attention_fwd(q, k, v, 1.0, False)
+    parts = [A.attention_fwd(q, k[:, :, a:b], v[:, :, a:b], 1.0, False) for a, b in ((0, 3), (3, 20))]
+    assert np.max(np.abs(np.mean([p[0] for p in parts], axis=0) - o)) > 1e-2
+
+
 # ------------------------------------------------------- finite differences ---
 
 @pytest.mark.parametrize("causal", [False, True])
