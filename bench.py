@@ -279,6 +279,11 @@ SWEEP = [  # (name, B, H, N, d, causal, multiplier, passes)
     ("wide-head-c", 2, 8, 16384, 256, True, 1.0, ("fwd", "bwd")),
 ]
 
+SWEEP_DECODE = [  # (name, B, H, Nq, Nk, d): split-KV forward, HBM-bound (K, V read once)
+    ("decode-64k-d128", 4, 16, 1, 65536, 128),
+    ("decode-16k-d64", 32, 16, 1, 16384, 64),
+]
+
 
 def naive_peak_bytes(q, k, v, do, scale):
     """Peak extra device memory of standard attention in PyTorch eager (S and P materialised
@@ -358,6 +363,31 @@ def run_sweep(reps: int = 20):
                               "peak_extra_MB_naive_eager": naive / 2**20,
                               "note": "extra device memory beyond q, k, v, dO for one fwd+bwd"}), flush=True)
         del q, k, v, do
+        torch.cuda.empty_cache()
+    hbm = peaks["hbm_gbs"]
+    for name, B, H, Nq, Nk, d in SWEEP_DECODE:
+        q = torch.from_numpy(I.normal_bf16((B, H, Nq, d), 1).view(np.int16)).view(torch.bfloat16).cuda()
+        k, v = (torch.from_numpy(I.normal_bf16((B, H, Nk, d), s).view(np.int16)).view(torch.bfloat16).cuda()
+                for s in (2, 3))
+        o, lse = fa.forward_splitkv(q, k, v)
+        ws = torch.empty(abi.fa_fwd_splitkv_workspace_bytes(B, H, Nq, Nk, d, 0), dtype=torch.uint8, device="cuda")
+        for _ in range(3):
+            fa.forward_splitkv(q, k, v, out=o, lse=lse, workspace=ws)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            fa.forward_splitkv(q, k, v, out=o, lse=lse, workspace=ws)
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / reps
+        nbytes = 2.0 * B * H * Nk * d * 2 + 2.0 * B * H * Nq * d * 2 + 4.0 * B * H * Nq
+        print(json.dumps({"config": name, "shape": [B, H, Nq, Nk, d], "pass": "fwd-splitkv", "ms": ms,
+                          "alg_gbs": nbytes / (ms * 1e-3) / 1e9, "frac_hbm": nbytes / (ms * 1e-3) / 1e9 / hbm,
+                          "splits": abi.fa_fwd_splitkv_num_splits(B, H, Nq, Nk, d, 0)}), flush=True)
+        if fa.status_check() != abi.FA_OK:
+            raise RuntimeError(f"device status not OK after {name}")
+        del q, k, v, o, lse, ws
         torch.cuda.empty_cache()
 
 
