@@ -162,6 +162,23 @@ def run_reference(args, rank, world):
 
 # ------------------------------------------------------------------ GPU arm ----
 
+def ranks_max(values, world: int, device="cpu"):
+    """Element-wise maximum of per-rank timings over all ranks (the slowest rank sets the
+    job's time); identity for a single process."""
+    if world == 1:
+        return list(values)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor(list(values), dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.tolist()]
+
+
+def job_throughput(flops_per_step_per_rank: float, world: int, max_ms_per_step: float) -> float:
+    """Whole-job TFLOP/s: every rank runs its own replica of the workload (weak scaling), so
+    the job processes world x the per-rank FLOPs in the slowest rank's time."""
+    return world * flops_per_step_per_rank / (max_ms_per_step * 1e-3) / 1e12
+
 def run_gpu(args, rank, world, local_rank):
     import numpy as np
     import torch
@@ -251,15 +268,7 @@ def run_gpu(args, rank, world, local_rank):
     barrier()
     e2e_ms = s2.elapsed_time(e2)
 
-    def world_max(x):
-        if world == 1:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
-
-    total_ms, e2e_ms = world_max(total_ms), world_max(e2e_ms)
-    fwd_ms, bwd_ms = world_max(fwd_ms), world_max(bwd_ms)
+    total_ms, e2e_ms, fwd_ms, bwd_ms = ranks_max([total_ms, e2e_ms, fwd_ms, bwd_ms], world, dev)
     return dict(total_ms=total_ms, fwd_ms=fwd_ms, bwd_ms=bwd_ms, e2e_ms=e2e_ms, h2d=h2d, d2h=d2h,
                 clocks=clocks.summary())
 
@@ -450,7 +459,7 @@ def main():
 
     fwd_f, bwd_f = step_flops(**WORKLOAD)
     ms = r["total_ms"] / args.steps
-    value = world * (fwd_f + bwd_f) / (ms * 1e-3) / 1e12
+    value = job_throughput(fwd_f + bwd_f, world, ms)
     peaks, src = load_peaks()
     sustained = peaks.get("bf16_tflops_sustained") or peaks["bf16_tflops"]
     bwd_tf = bwd_f / (r["bwd_ms"] * 1e-3) / 1e12
