@@ -354,6 +354,14 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
         }
         if (!mbar_wait(bar(L::kBarDSReady), ph, wc)) { ok = false; break; }
         tc_fence_after_sync();
+        // dQ_i first, with its own completion signal, so the drain warps read it while dK_i
+        // runs and dP_{i+1} (which reuses its columns) can follow dK_i without a gap.
+#pragma unroll
+        for (int kk = 0; kk < kTile / 16; ++kk) {
+          mma_ss(tmem + L::kColDP, sdesc_sw128(sdS + kk * (16 * 128), kTile * 128, 1024),
+                 sdesc_sw128(sK + kk * (16 * 128), kTile * 128, 1024), kIdDQ, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(bar(L::kBarDQFull));
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk) {
           const uint32_t a_off = (kk >> 2) * (kTile * 128) + (kk & 3) * 32;  // dS^T K-major
@@ -361,12 +369,6 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                  sdesc_sw128(sQ(st) + kk * (16 * 128), kTile * 128, 1024), kIdAcc,
                  (it > 0 || kk > 0) ? 1u : 0u);
         }
-#pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk) {
-          mma_ss(tmem + L::kColDP, sdesc_sw128(sdS + kk * (16 * 128), kTile * 128, 1024),
-                 sdesc_sw128(sK + kk * (16 * 128), kTile * 128, 1024), kIdDQ, kk > 0 ? 1u : 0u);
-        }
-        mma_commit(bar(L::kBarDQFull));
         mma_commit(bar(L::kBarDSFree));
         mma_commit(bar(L::kBarQEmpty + st));
         // dP_{i+1} overwrites the dQ_i tile: wait until the drain warps have read it.
