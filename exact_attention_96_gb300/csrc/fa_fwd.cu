@@ -78,7 +78,7 @@ struct FwdLayout {
   static_assert(D % 64 == 0 && BC % 32 == 0 && BC <= 256, "tile shape");
 };
 
-template <int D, int BC, int NS, bool CAUSAL>
+template <int D, int BC, int NS, bool CAUSAL, bool SPLIT>
 __global__ void __launch_bounds__(kThreads, 1)
 fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
               const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
@@ -98,9 +98,9 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
   const int Nk = args.Nk;  // keys
   const int n_kv_all = (Nk + BC - 1) / BC;
   // this CTA's key tiles: [t_begin, t_begin + nkv) (split mode: one range per blockIdx.z)
-  const int t_begin = int(blockIdx.z) * args.tiles_per_split;
+  const int t_begin = SPLIT ? int(blockIdx.z) * args.tiles_per_split : 0;
   const int nkv = CAUSAL ? min(n_kv_all, (q0 + kBM + BC - 1) / BC)
-                         : min(n_kv_all - t_begin, args.tiles_per_split);
+                         : (SPLIT ? min(n_kv_all - t_begin, args.tiles_per_split) : n_kv_all);
 
   auto bar = [&](int i) -> uint32_t { return base + L::kBarOff + 8u * uint32_t(i); };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
@@ -328,7 +328,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
 
     // ------------------------------------------------------------ epilogue ----
     const bool fin = ok && __all_sync(0xffffffffu, mbar_wait(bar(L::kBarOFinal), 0, wc));
-    const bool split_mode = args.o_part != nullptr;
+    constexpr bool split_mode = SPLIT;
     if (fin && split_mode) {
       // partial output of this key range: O normalised by its own l (fp32) and its LSE
       tc_fence_after_sync();
@@ -393,7 +393,9 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
 template <int D, int BC, int NS, bool CAUSAL>
 cudaError_t launch_cfg(const Maps& m, const FwdArgs& a, cudaStream_t s) {
   using L = FwdLayout<D, BC, NS>;
-  auto kern = fa_fwd_kernel<D, BC, NS, CAUSAL>;
+  // split-KV partial outputs are a separate instantiation (non-causal only), so the square
+  // problem's kernel carries none of that code
+  auto kern = a.o_part != nullptr ? fa_fwd_kernel<D, BC, NS, false, true> : fa_fwd_kernel<D, BC, NS, CAUSAL, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemAlloc);
   if (e != cudaSuccess) return e;
   dim3 grid(a.n_q_tiles, a.BH, a.num_splits);
