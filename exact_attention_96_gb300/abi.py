@@ -32,6 +32,10 @@ SIGNATURES = {
     "fa_fwd_splitkv": (_c_int, [_c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_void_p,
                                 _c_int, _c_int, _c_int, _c_int, _c_int, _c_float, _c_int,
                                 _c_void_p, _c_size_t, _c_void_p]),
+    "fa_fwd_partial": (_c_int, [_c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_void_p,
+                                _c_int, _c_int, _c_int, _c_int, _c_int, _c_float, _c_int, _c_void_p]),
+    "fa_merge_partials": (_c_int, [_c_void_p, _c_void_p, _c_int, ctypes.c_longlong, _c_int,
+                                   _c_void_p, _c_void_p, _c_void_p]),
     "fa_bwd_workspace_bytes": (_c_size_t, [_c_int, _c_int, _c_int, _c_int]),
     "fa_bwd": (_c_int, [_c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_void_p,
                         _c_void_p, _c_void_p, _c_void_p,
@@ -95,6 +99,14 @@ def fa_fwd_splitkv_num_splits(B, H, Nq, Nk, d, num_splits) -> int:
 
 def fa_fwd_splitkv(q, k, v, o, lse, B, H, Nq, Nk, d, scale, num_splits, ws, ws_bytes, stream) -> int:
     return load().fa_fwd_splitkv(q, k, v, o, lse, B, H, Nq, Nk, d, scale, num_splits, ws, ws_bytes, stream)
+
+
+def fa_fwd_partial(q, k, v, o_part, lse_part, B, H, Nq, Nk, d, scale, causal, stream) -> int:
+    return load().fa_fwd_partial(q, k, v, o_part, lse_part, B, H, Nq, Nk, d, scale, int(causal), stream)
+
+
+def fa_merge_partials(o_parts, lse_parts, num_parts, rows, d, o, lse, stream) -> int:
+    return load().fa_merge_partials(o_parts, lse_parts, num_parts, rows, d, o, lse, stream)
 
 
 def fa_bwd_workspace_bytes(B, H, N, d) -> int:

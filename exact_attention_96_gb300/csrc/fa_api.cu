@@ -259,6 +259,57 @@ fa_status fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, f
   return e == cudaSuccess ? FA_OK : cuda_fail(e);
 }
 
+fa_status fa_fwd_partial(const void* q, const void* k, const void* v, float* o_part, float* lse_part, int B,
+                         int H, int Nq, int Nk, int d, float scale, int causal, fa_stream_t stream) {
+  if (!q || !k || !v || !o_part || !lse_part) return FA_ERR_INVALID_ARG;
+  fa_status st = check_sizes(B, H, Nq, d);
+  if (st != FA_OK) return st;
+  if ((st = check_sizes(B, H, Nk, d)) != FA_OK) return st;
+  if ((st = check_scale(scale)) != FA_OK) return st;
+  if (causal && Nq != Nk) return FA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o_part) || !aligned16(lse_part))
+    return FA_ERR_MISALIGNED;
+  int dev = 0;
+  int* err = nullptr;
+  if ((st = device_setup(&dev, &err)) != FA_OK) return st;
+  const int BH = B * H;
+  const int kv_rows = fa::fwd_kv_tile(d);
+  fa::Maps maps;
+  if (!encode_bf16_rows(&maps.q, q, BH, Nq, d, 128) || !encode_bf16_rows(&maps.k, k, BH, Nk, d, kv_rows) ||
+      !encode_bf16_rows(&maps.v, v, BH, Nk, d, kv_rows) || !encode_bf16_rows(&maps.o, q, BH, Nq, d, 128))
+    return FA_ERR_CUDA;
+  fa::FwdArgs a;
+  a.lse = lse_part;
+  a.N = Nq;
+  a.Nk = Nk;
+  a.num_splits = 1;
+  a.tiles_per_split = (Nk + kv_rows - 1) / kv_rows;
+  a.o_part = o_part;
+  a.lse_part = lse_part;
+  a.BH = BH;
+  a.n_q_tiles = (Nq + 127) / 128;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.wait_limit_ns = g_wait_limit_ns.load();
+  a.err_word = err;
+  a.withhold_k_tile = -1;
+  const cudaError_t e = fa::launch_fwd(maps, a, d, causal != 0, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : cuda_fail(e);
+}
+
+fa_status fa_merge_partials(const float* o_parts, const float* lse_parts, int num_parts, long long rows, int d,
+                            void* o, float* lse, fa_stream_t stream) {
+  if (!o_parts || !lse_parts || !o || !lse || num_parts < 1 || rows < 1) return FA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128 && d != 256) return FA_ERR_UNSUPPORTED;
+  if (!aligned16(o_parts) || !aligned16(lse_parts) || !aligned16(o) || !aligned16(lse)) return FA_ERR_MISALIGNED;
+  int dev = 0;
+  int* err = nullptr;
+  fa_status st = device_setup(&dev, &err);
+  if (st != FA_OK) return st;
+  const cudaError_t e = fa::launch_splitkv_combine(o_parts, lse_parts, static_cast<uint16_t*>(o), lse, rows,
+                                                   num_parts, d, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : cuda_fail(e);
+}
+
 size_t fa_bwd_workspace_bytes(int B, int H, int N, int d) {
   if (check_sizes(B, H, N, d) != FA_OK) return 0;
   return ws_layout(B, H, N, d).total;

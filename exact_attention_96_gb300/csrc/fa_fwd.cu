@@ -395,7 +395,7 @@ cudaError_t launch_cfg(const Maps& m, const FwdArgs& a, cudaStream_t s) {
   using L = FwdLayout<D, BC, NS>;
   // split-KV partial outputs are a separate instantiation (non-causal only), so the square
   // problem's kernel carries none of that code
-  auto kern = a.o_part != nullptr ? fa_fwd_kernel<D, BC, NS, false, true> : fa_fwd_kernel<D, BC, NS, CAUSAL, false>;
+  auto kern = a.o_part != nullptr ? fa_fwd_kernel<D, BC, NS, CAUSAL, true> : fa_fwd_kernel<D, BC, NS, CAUSAL, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemAlloc);
   if (e != cudaSuccess) return e;
   dim3 grid(a.n_q_tiles, a.BH, a.num_splits);

@@ -81,6 +81,27 @@ fa_status fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, f
                          void* workspace, size_t workspace_bytes, fa_stream_t stream);
 
 /*
+ * Building blocks of attention over a sequence held in shards (ring attention, "Flash
+ * Attention 原理与实践" §5.2: key/value shards pass around a ring of workers, each worker runs
+ * FlashAttention of its queries against the shard it holds, and the partial results are
+ * merged by log-sum-exp).
+ *
+ * fa_fwd_partial: attention of q [B,H,Nq,d] against one key/value block k, v [B,H,Nk,d]
+ *   alone, written as fp32 o_part [B,H,Nq,d] (normalised within the block) and fp32 lse_part
+ *   [B,H,Nq] (log-sum-exp over the block).  causal != 0 requires Nq == Nk (the diagonal block
+ *   of a causal problem: key j hidden from query i when j > i).
+ * fa_merge_partials: o_parts [num_parts][rows][d] and lse_parts [num_parts][rows] (rows =
+ *   B*H*Nq, one entry per partial) -> bf16 o [rows][d] and fp32 lse [rows] of the union of
+ *   the blocks.  Every row must have at least one block with a visible key.
+ * Both are asynchronous on `stream`; errors as for fa_fwd.
+ */
+fa_status fa_fwd_partial(const void* q, const void* k, const void* v, float* o_part, float* lse_part,
+                         int B, int H, int Nq, int Nk, int d, float scale, int causal,
+                         fa_stream_t stream);
+fa_status fa_merge_partials(const float* o_parts, const float* lse_parts, int num_parts,
+                            long long rows, int d, void* o, float* lse, fa_stream_t stream);
+
+/*
  * Bytes of device workspace fa_bwd needs: D [B,H,N] fp32 followed (at a 256-byte aligned
  * offset) by the fp32 dQ accumulator [B,H,N,d].  Returns 0 for invalid sizes.
  */
