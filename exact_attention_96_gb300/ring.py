@@ -1,7 +1,7 @@
-"""Ring attention over sequence shards, emulated on one GPU ("Flash Attention 原理与实践"
-§5.2: the key/value sequence is split across workers, shards pass around a ring, each worker
-runs FlashAttention of its own queries against the shard it currently holds, and the partial
-results are merged with log-sum-exp).
+"""Ring attention over sequence shards, forward and backward, emulated on one GPU ("Flash
+Attention 原理与实践" §5.2: the key/value sequence is split across workers, shards pass around
+a ring, each worker runs FlashAttention of its own queries against the shard it currently
+holds, and the partial results are merged with log-sum-exp).
 
 On a ring of `world` workers, at hop t worker r holds the key/value shard that started on
 worker (r - t) mod world.  With a causal mask worker r needs only shards s <= r, the shard
@@ -61,3 +61,35 @@ def ring_attention_forward(q, k, v, world: int, causal: bool = False, scale: flo
         o[:, :, r * ns:(r + 1) * ns] = o_r
         lse[:, :, r * ns:(r + 1) * ns] = lse_r
     return o, lse
+
+
+def ring_attention_backward(q, k, v, o, do, lse, world: int, causal: bool = False,
+                            scale: float | None = None):
+    """dQ, dK, dV of ring attention.  With the global LSE (from the forward) every
+    probability is fixed, so the contribution of query shard r and key/value shard s is
+    exactly the backward pass of that block pair (fa_bwd with O_r, dO_r and LSE_r; the
+    diagonal pair causal, later shards skipped).  Worker r accumulates dQ_r over the shards
+    it sees; dK_s, dV_s collect the contributions of every worker that saw shard s (on a
+    real ring they travel back with the shard).  The sums are fp32."""
+    from . import attention as fa  # local import: attention imports nothing from here
+
+    B, H, N, d = q.shape
+    if N % world:
+        raise ValueError("sequence length must be a multiple of the ring size")
+    ns = N // world
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    shard = lambda t, i: t[:, :, i * ns:(i + 1) * ns].contiguous()  # noqa: E731
+    dq = torch.zeros(q.shape, dtype=torch.float32, device=q.device)
+    dk = torch.zeros(k.shape, dtype=torch.float32, device=q.device)
+    dv = torch.zeros(v.shape, dtype=torch.float32, device=q.device)
+    ws = torch.empty(fa.workspace_bytes(B, H, ns, d), dtype=torch.uint8, device=q.device)
+    grads = tuple(torch.empty((B, H, ns, d), dtype=q.dtype, device=q.device) for _ in range(3))
+    for r in range(world):
+        q_r, o_r, do_r, lse_r = shard(q, r), shard(o, r), shard(do, r), shard(lse, r)
+        for _, s, diag in ring_hops(r, world, causal):
+            g_q, g_k, g_v = fa.backward(q_r, shard(k, s), shard(v, s), o_r, do_r, lse_r,
+                                        causal=causal and diag, scale=scale, workspace=ws, grads=grads)
+            dq[:, :, r * ns:(r + 1) * ns] += g_q.float()
+            dk[:, :, s * ns:(s + 1) * ns] += g_k.float()
+            dv[:, :, s * ns:(s + 1) * ns] += g_v.float()
+    return dq.to(q.dtype), dk.to(k.dtype), dv.to(v.dtype)
