@@ -27,6 +27,7 @@ attention       forward / backward definitions, whole tensors or sampled rows / 
 online_softmax  the streaming (running max, running sum) recurrence and the tiled
                 forward in both loop orders the pages describe
 io_model        FLOP and HBM-byte counters used by the pages' worked examples
+philox          the counter-based generator behind the dropout mask
 
 Parity status: every function here is pinned by tests under ``tests/`` (see
 ``tests/test_oracle_pins.py``) except the numbers of the online-softmax worked example
@@ -34,4 +35,4 @@ in "FlashAttention 与显存" §08, whose eight input scores are not printed: on
 invariant (blockwise == full-row) is checked, its printed values are parity unpinned.
 """
 
-from . import attention, online_softmax, io_model  # noqa: F401
+from . import attention, online_softmax, io_model, philox  # noqa: F401

@@ -27,11 +27,19 @@ from Q, K, V block by block).  With dO the upstream gradient of O:
 S and P are materialised for a chunk of query rows at a time, over the full key
 length, which is still the plain definition (no online rescaling), and keeps the
 memory bounded for N = 65536.
+
+Dropout (optional, p > 0; "FlashAttention 与显存" §07, §09): after the softmax each
+probability is kept with probability 1 - p and scaled by 1/(1 - p), Z = keep / (1 - p), the
+mask drawn from the counter-based generator in ``philox`` (so it can be regenerated instead
+of stored).  O = (P * Z) V; LSE is that of the undropped P.  Backward: dV = (P * Z)^T dO,
+dP = dO V^T, dS = P * (dP * Z - D) with D = rowsum(dO * O) (still = rowsum(P * Z * dP)).
 """
 
 from __future__ import annotations
 
 import numpy as np
+
+from . import philox
 
 __all__ = [
     "bf16_bits_to_f64",
@@ -80,7 +88,13 @@ def _softmax_rows(s: np.ndarray):
     return e / l[:, None], m, l
 
 
-def attention_fwd(q, k, v, scale: float, causal: bool, row_chunk: int = 512):
+def _dropout_z(bh, rows, n_keys, p, seed):
+    keep = philox.dropout_keep(bh, rows, np.arange(n_keys), p, seed)
+    return keep / (1.0 - p)
+
+
+def attention_fwd(q, k, v, scale: float, causal: bool, row_chunk: int = 512,
+                  dropout_p: float = 0.0, seed: int = 0):
     """O [B,H,N,d] and LSE [B,H,N] in fp64 for fp64 inputs [B,H,N,d]."""
     q = np.asarray(q, dtype=np.float64)
     k = np.asarray(k, dtype=np.float64)
@@ -95,6 +109,8 @@ def attention_fwd(q, k, v, scale: float, causal: bool, row_chunk: int = 512):
                 rows = np.arange(r0, r1)
                 s = scores(q[b, h, r0:r1], k[b, h], scale, causal, rows)
                 p, m, l = _softmax_rows(s)
+                if dropout_p > 0:
+                    p = p * _dropout_z(b * H + h, rows, k.shape[2], dropout_p, seed)
                 o[b, h, r0:r1] = p @ v[b, h]
                 lse[b, h, r0:r1] = m + np.log(l)
     return o, lse
@@ -114,10 +130,12 @@ def attention_fwd_rows(q_head, k_head, v_head, scale: float, causal: bool, rows)
     return p @ np.asarray(v_head, np.float64), m + np.log(l)
 
 
-def attention_bwd_head(q, k, v, do, scale: float, causal: bool, row_chunk: int = 512):
+def attention_bwd_head(q, k, v, do, scale: float, causal: bool, row_chunk: int = 512,
+                       dropout_p: float = 0.0, seed: int = 0, bh: int = 0):
     """dQ, dK, dV [N, d] and D [N] for one head, all fp64 [N, d] inputs.
 
-    D is rowsum(dO * O) with O from this same definition.
+    D is rowsum(dO * O) with O from this same definition.  With dropout the mask is that of
+    head index ``bh`` (= batch * H + head).
     """
     q = np.asarray(q, np.float64)
     k = np.asarray(k, np.float64)
@@ -133,18 +151,20 @@ def attention_bwd_head(q, k, v, do, scale: float, causal: bool, row_chunk: int =
         rows = np.arange(r0, r1)
         s = scores(q[r0:r1], k, scale, causal, rows)
         p, _, _ = _softmax_rows(s)
-        o = p @ v
-        dv += p.T @ do[r0:r1]
+        z = _dropout_z(bh, rows, k.shape[0], dropout_p, seed) if dropout_p > 0 else 1.0
+        o = (p * z) @ v
+        dv += (p * z).T @ do[r0:r1]
         dp = do[r0:r1] @ v.T
         drow = np.sum(do[r0:r1] * o, axis=1)
-        ds = p * (dp - drow[:, None])
+        ds = p * (dp * z - drow[:, None])
         dq[r0:r1] = scale * (ds @ k)
         dk += scale * (ds.T @ q[r0:r1])
         dvec[r0:r1] = drow
     return dq, dk, dv, dvec
 
 
-def attention_bwd(q, k, v, do, scale: float, causal: bool, row_chunk: int = 512):
+def attention_bwd(q, k, v, do, scale: float, causal: bool, row_chunk: int = 512,
+                  dropout_p: float = 0.0, seed: int = 0):
     """dQ, dK, dV [B,H,N,d] and D [B,H,N] for fp64 inputs [B,H,N,d]."""
     q = np.asarray(q, np.float64)
     B, H, N, d = q.shape
@@ -155,7 +175,8 @@ def attention_bwd(q, k, v, do, scale: float, causal: bool, row_chunk: int = 512)
     for b in range(B):
         for h in range(H):
             dq[b, h], dk[b, h], dv[b, h], dvec[b, h] = attention_bwd_head(
-                q[b, h], k[b, h], v[b, h], do[b, h], scale, causal, row_chunk)
+                q[b, h], k[b, h], v[b, h], do[b, h], scale, causal, row_chunk,
+                dropout_p, seed, b * H + h)
     return dq, dk, dv, dvec
 
 

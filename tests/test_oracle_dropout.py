@@ -1,0 +1,102 @@
+"""Pins of the oracle's dropout (mask generator and dropout arithmetic).
+
+The generator is checked by its statistics and its dependence on every counter field; the
+arithmetic by reduction to the plain path at p = 0, by unbiasedness over seeds, by central
+finite differences at a fixed mask, and by torch (softmax and autograd) applied to P * Z."""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+import torch.nn.functional as F
+
+from oracle import attention as A
+from oracle import philox
+
+
+def rnd(shape, seed):
+    return np.random.default_rng(seed).standard_normal(shape)
+
+
+@pytest.mark.parametrize("p", [0.1, 0.5, 0.9])
+def test_keep_rate(p):
+    keep = philox.dropout_keep(3, np.arange(256), np.arange(4096), p, seed=12345)
+    n = keep.size
+    sigma = math.sqrt(n * p * (1 - p))
+    assert abs(keep.sum() - n * (1 - p)) < 5 * sigma
+
+
+def test_mask_depends_on_every_coordinate():
+    base = philox.dropout_keep(0, np.arange(64), np.arange(64), 0.5, seed=7)
+    assert not np.array_equal(base, philox.dropout_keep(1, np.arange(64), np.arange(64), 0.5, seed=7))
+    assert not np.array_equal(base, philox.dropout_keep(0, np.arange(64), np.arange(64), 0.5, seed=8))
+    assert not np.array_equal(base, philox.dropout_keep(0, np.arange(64), np.arange(64), 0.5, seed=7 << 32))
+    # neighbouring rows and the four keys that share one generator call are not copies
+    assert np.mean(base[1:] == base[:-1]) < 0.6
+    assert np.mean(base[:, 1:] == base[:, :-1]) < 0.6
+    assert np.all(philox.dropout_keep(0, np.arange(4), np.arange(4), 0.0, seed=1))
+
+
+def test_zero_dropout_is_the_plain_path():
+    q, k, v, do = (rnd((1, 2, 9, 4), s) for s in (1, 2, 3, 4))
+    for causal in (False, True):
+        a = A.attention_fwd(q, k, v, 0.5, causal)
+        b = A.attention_fwd(q, k, v, 0.5, causal, dropout_p=0.0, seed=99)
+        assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+        ga = A.attention_bwd(q, k, v, do, 0.5, causal)
+        gb = A.attention_bwd(q, k, v, do, 0.5, causal, dropout_p=0.0, seed=99)
+        assert all(np.array_equal(x, y) for x, y in zip(ga, gb))
+
+
+def test_dropout_is_unbiased_over_seeds():
+    q, k, v = (rnd((1, 1, 6, 3), s) for s in (5, 6, 7))
+    o, _ = A.attention_fwd(q, k, v, 0.8, False)
+    acc = np.zeros_like(o)
+    n = 3000
+    for seed in range(n):
+        acc += A.attention_fwd(q, k, v, 0.8, False, dropout_p=0.3, seed=seed)[0]
+    assert np.max(np.abs(acc / n - o)) < 0.05
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_dropout_gradients_match_finite_differences(causal):
+    N, d, p, seed = 6, 3, 0.4, 2024
+    q, k, v, do = (rnd((N, d), s) for s in (8, 9, 10, 11))
+    h = 1e-6
+
+    def loss(q_, k_, v_):
+        o, _ = A.attention_fwd(q_[None, None], k_[None, None], v_[None, None], 0.7, causal,
+                               dropout_p=p, seed=seed)
+        return float(np.sum(o[0, 0] * do))
+
+    grads = A.attention_bwd_head(q, k, v, do, 0.7, causal, dropout_p=p, seed=seed, bh=0)
+    for which, g in enumerate(grads[:3]):
+        num = np.zeros_like(g)
+        for idx in np.ndindex(*g.shape):
+            a = [q.copy(), k.copy(), v.copy()]
+            b = [q.copy(), k.copy(), v.copy()]
+            a[which][idx] += h
+            b[which][idx] -= h
+            num[idx] = (loss(*a) - loss(*b)) / (2 * h)
+        assert np.linalg.norm(num - g) / np.linalg.norm(g) < 1e-7, which
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_dropout_matches_torch_on_the_same_mask(causal):
+    B, H, N, d, p, seed = 2, 2, 11, 4, 0.25, 5
+    q, k, v, do = (rnd((B, H, N, d), s) for s in (12, 13, 14, 15))
+    o, lse = A.attention_fwd(q, k, v, 0.6, causal, dropout_p=p, seed=seed)
+    dq, dk, dv, _ = A.attention_bwd(q, k, v, do, 0.6, causal, dropout_p=p, seed=seed)
+    z = np.stack([np.stack([philox.dropout_keep(b * H + h, np.arange(N), np.arange(N), p, seed)
+                            for h in range(H)]) for b in range(B)]) / (1 - p)
+    tq, tk, tv = (torch.tensor(x, requires_grad=True) for x in (q, k, v))
+    s = 0.6 * tq @ tk.transpose(-1, -2)
+    if causal:
+        s = s.masked_fill(torch.ones(N, N, dtype=torch.bool).triu(1), float("-inf"))
+    to = (torch.softmax(s, dim=-1) * torch.tensor(z)) @ tv
+    to.backward(torch.tensor(do))
+    assert np.max(np.abs(o - to.detach().numpy())) < 1e-12
+    assert np.max(np.abs(lse - torch.logsumexp(s, -1).detach().numpy())) < 1e-12
+    for g, t in ((dq, tq), (dk, tk), (dv, tv)):
+        assert np.max(np.abs(g - t.grad.numpy())) < 1e-11
