@@ -29,9 +29,9 @@ length, which is still the plain definition (no online rescaling), and keeps the
 memory bounded for N = 65536.
 
 Dropout (optional, p > 0; "FlashAttention 与显存" §07, §09): after the softmax each
-probability is kept with probability 1 - p and scaled by 1/(1 - p), Z = keep / (1 - p), the
-mask drawn from the counter-based generator in ``philox`` (so it can be regenerated instead
-of stored).  O = (P * Z) V; LSE is that of the undropped P.  Backward: dV = (P * Z)^T dO,
+probability is kept with probability 1 - p and scaled by the inverse of that probability,
+Z = keep * philox.keep_scale(p) (p quantised to multiples of 2^-16), the mask drawn from the
+counter-based generator in ``philox`` (so it can be regenerated instead of stored).  O = (P * Z) V; LSE is that of the undropped P.  Backward: dV = (P * Z)^T dO,
 dP = dO V^T, dS = P * (dP * Z - D) with D = rowsum(dO * O) (still = rowsum(P * Z * dP)).
 """
 
@@ -90,7 +90,7 @@ def _softmax_rows(s: np.ndarray):
 
 def _dropout_z(bh, rows, n_keys, p, seed):
     keep = philox.dropout_keep(bh, rows, np.arange(n_keys), p, seed)
-    return keep / (1.0 - p)
+    return keep * philox.keep_scale(p)
 
 
 def attention_fwd(q, k, v, scale: float, causal: bool, row_chunk: int = 512,

@@ -9,11 +9,14 @@ halves), then
 and the key is bumped by the Weyl constants (0x9E3779B9, 0xBB67AE85) between rounds.
 
 Dropout mask ("FlashAttention 与显存" §07/§09: dropout is fused into the kernel and its mask is
-not stored; the backward pass regenerates it from the generator's state): element (bh, i, j)
-of the attention matrix (bh = batch*H + head, i = query, j = key) reads word j % 4 of
-Philox(counter = (j // 4, i, bh, 0), key = (seed & 0xffffffff, seed >> 32)); the element is
-kept when that word is >= threshold(p) = min(round(p * 2^32), 2^32 - 1), and kept elements are
-scaled by 1 / (1 - p).
+not stored; the backward pass regenerates it from the generator's state).  The pages fix no
+generator or bit layout; this one is chosen so that one generator call serves eight elements:
+element (bh, i, j) of the attention matrix (bh = batch*H + head, i = query, j = key) reads
+the 16-bit half (j % 2: 0 = low half) of word (j % 8) // 2 of
+Philox(counter = (j // 8, i, bh, 0), key = (seed & 0xffffffff, seed >> 32)).  The element is
+kept when that half is >= t = min(round(p * 2^16), 2^16 - 1), i.e. with probability
+(2^16 - t) / 2^16, and kept elements are scaled by the inverse of that probability, so the
+mask's expectation is exactly 1 (p is quantised to multiples of 2^-16).
 """
 
 from __future__ import annotations
@@ -45,17 +48,28 @@ def philox4x32_10(c0, c1, c2, c3, k0, k1):
 
 
 def keep_threshold(p: float) -> int:
-    return min(int(round(p * 2.0 ** 32)), 2 ** 32 - 1)
+    """16-bit threshold t: an element is kept when its 16-bit draw is >= t."""
+    if not 0.0 <= p < 1.0:
+        raise ValueError("dropout probability must be in [0, 1)")
+    return min(int(round(p * 65536.0)), 65535)
+
+
+def keep_scale(p: float) -> float:
+    """Inverse of the keep probability (2^16 - t) / 2^16."""
+    return 65536.0 / (65536 - keep_threshold(p))
 
 
 def dropout_keep(bh: int, rows, cols, p: float, seed: int) -> np.ndarray:
     """Boolean keep mask [len(rows), len(cols)] for head index bh."""
     rows = np.asarray(rows, np.uint64)[:, None]
     cols = np.asarray(cols, np.uint64)[None, :]
-    c0 = np.broadcast_to(cols >> np.uint64(2), (rows.shape[0], cols.shape[1]))
+    t = keep_threshold(p)
+    c0 = np.broadcast_to(cols >> np.uint64(3), (rows.shape[0], cols.shape[1]))
     c1 = np.broadcast_to(rows, c0.shape)
     words = philox4x32_10(c0, c1, np.full(c0.shape, bh, np.uint64), np.zeros(c0.shape, np.uint64),
                           seed & 0xFFFFFFFF, (seed >> 32) & 0xFFFFFFFF)
-    sel = np.broadcast_to(cols & np.uint64(3), c0.shape)
+    sel = np.broadcast_to((cols & np.uint64(7)) >> np.uint64(1), c0.shape)
     w = np.choose(sel.astype(np.int64), words)
-    return w >= np.uint32(keep_threshold(p)) if p > 0 else np.ones(c0.shape, bool)
+    half = np.broadcast_to(cols & np.uint64(1), c0.shape).astype(np.uint32)
+    draw = (w >> (np.uint32(16) * half)) & np.uint32(0xFFFF)
+    return draw >= np.uint32(t) if p > 0 else np.ones(c0.shape, bool)

@@ -32,7 +32,7 @@ def test_mask_depends_on_every_coordinate():
     assert not np.array_equal(base, philox.dropout_keep(1, np.arange(64), np.arange(64), 0.5, seed=7))
     assert not np.array_equal(base, philox.dropout_keep(0, np.arange(64), np.arange(64), 0.5, seed=8))
     assert not np.array_equal(base, philox.dropout_keep(0, np.arange(64), np.arange(64), 0.5, seed=7 << 32))
-    # neighbouring rows and the four keys that share one generator call are not copies
+    # neighbouring rows and the eight keys that share one generator call are not copies
     assert np.mean(base[1:] == base[:-1]) < 0.6
     assert np.mean(base[:, 1:] == base[:, :-1]) < 0.6
     assert np.all(philox.dropout_keep(0, np.arange(4), np.arange(4), 0.0, seed=1))
@@ -89,7 +89,7 @@ def test_dropout_matches_torch_on_the_same_mask(causal):
     o, lse = A.attention_fwd(q, k, v, 0.6, causal, dropout_p=p, seed=seed)
     dq, dk, dv, _ = A.attention_bwd(q, k, v, do, 0.6, causal, dropout_p=p, seed=seed)
     z = np.stack([np.stack([philox.dropout_keep(b * H + h, np.arange(N), np.arange(N), p, seed)
-                            for h in range(H)]) for b in range(B)]) / (1 - p)
+                            for h in range(H)]) for b in range(B)]) * philox.keep_scale(p)
     tq, tk, tv = (torch.tensor(x, requires_grad=True) for x in (q, k, v))
     s = 0.6 * tq @ tk.transpose(-1, -2)
     if causal:
@@ -100,3 +100,24 @@ def test_dropout_matches_torch_on_the_same_mask(causal):
     assert np.max(np.abs(lse - torch.logsumexp(s, -1).detach().numpy())) < 1e-12
     for g, t in ((dq, tq), (dk, tk), (dv, tv)):
         assert np.max(np.abs(g - t.grad.numpy())) < 1e-11
+
+
+def test_keep_probability_times_scale_is_one():
+    # E[Z] = 1 exactly: t of the 2^16 draws are dropped, the rest scaled by 2^16 / (2^16 - t)
+    for p in (0.0, 1e-6, 0.1, 0.25, 0.5, 0.9, 0.99999):
+        t = philox.keep_threshold(p)
+        assert abs(t - p * 65536) <= 0.5
+        assert (65536 - t) / 65536 * philox.keep_scale(p) == 1.0
+    with pytest.raises(ValueError):
+        philox.keep_threshold(1.0)
+
+
+def test_every_sixteen_bit_draw_pattern_is_used():
+    # over many calls the 16-bit draws of all eight slots are uniform: the slot-wise keep rates
+    # at p = 0.5 agree, so no slot reads a constant or a shared half
+    keep = philox.dropout_keep(5, np.arange(512), np.arange(512), 0.5, seed=99)
+    rates = keep.reshape(512, 64, 8).mean(axis=(0, 1))
+    sigma = math.sqrt(0.25 / (512 * 64))
+    assert np.all(np.abs(rates - 0.5) < 5 * sigma)
+    # the two halves of one word are not the same draw
+    assert np.mean(keep[:, 0::2] == keep[:, 1::2]) < 0.55
