@@ -41,6 +41,14 @@ SIGNATURES = {
                         _c_void_p, _c_void_p, _c_void_p,
                         _c_int, _c_int, _c_int, _c_int, _c_float, _c_int,
                         _c_void_p, _c_size_t, _c_void_p]),
+    "fa_fwd_dropout": (_c_int, [_c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_void_p,
+                                _c_int, _c_int, _c_int, _c_int, _c_float, _c_int,
+                                ctypes.c_double, ctypes.c_ulonglong, _c_void_p]),
+    "fa_bwd_dropout": (_c_int, [_c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_void_p,
+                                _c_void_p, _c_void_p, _c_void_p,
+                                _c_int, _c_int, _c_int, _c_int, _c_float, _c_int,
+                                ctypes.c_double, ctypes.c_ulonglong,
+                                _c_void_p, _c_size_t, _c_void_p]),
     "fa_bwd_noalloc": (_c_int, [_c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_void_p,
                                 _c_void_p, _c_void_p, _c_void_p,
                                 _c_int, _c_int, _c_int, _c_int, _c_float, _c_int, _c_void_p]),
@@ -116,6 +124,17 @@ def fa_bwd_workspace_bytes(B, H, N, d) -> int:
 def fa_bwd(q, k, v, o, do, lse, dq, dk, dv, B, H, N, d, scale, causal, ws, ws_bytes, stream) -> int:
     return load().fa_bwd(q, k, v, o, do, lse, dq, dk, dv, B, H, N, d, scale, int(causal),
                          ws, ws_bytes, stream)
+
+
+def fa_fwd_dropout(q, k, v, o, lse, B, H, N, d, scale, causal, dropout_p, seed, stream) -> int:
+    return load().fa_fwd_dropout(q, k, v, o, lse, B, H, N, d, scale, int(causal), float(dropout_p),
+                                 int(seed) & 0xFFFFFFFFFFFFFFFF, stream)
+
+
+def fa_bwd_dropout(q, k, v, o, do, lse, dq, dk, dv, B, H, N, d, scale, causal, dropout_p, seed,
+                   ws, ws_bytes, stream) -> int:
+    return load().fa_bwd_dropout(q, k, v, o, do, lse, dq, dk, dv, B, H, N, d, scale, int(causal),
+                                 float(dropout_p), int(seed) & 0xFFFFFFFFFFFFFFFF, ws, ws_bytes, stream)
 
 
 def fa_bwd_noalloc(q, k, v, o, do, lse, dq, dk, dv, B, H, N, d, scale, causal, stream) -> int:

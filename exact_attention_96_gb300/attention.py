@@ -27,17 +27,23 @@ def _stream(t: torch.Tensor) -> int:
     return torch.cuda.current_stream(t.device).cuda_stream
 
 
-def forward(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None):
-    """O, LSE = attention(q, k, v); writes into `out` / `lse` when given."""
+def forward(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None,
+            dropout_p: float = 0.0, seed: int = 0):
+    """O, LSE = attention(q, k, v); writes into `out` / `lse` when given.  dropout_p > 0
+    applies the generator-defined dropout mask of (seed, head, query, key) (fa_fwd_dropout)."""
     _check_qkv(q, k, v)
     B, H, N, d = q.shape
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
     o = torch.empty_like(q) if out is None else out
     l = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if lse is None else lse
     with torch.cuda.device(q.device):
-        st = abi.fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), l.data_ptr(),
-                        B, H, N, d, scale, causal, _stream(q))
-    abi.check("fa_fwd", st)
+        if dropout_p > 0:
+            st = abi.fa_fwd_dropout(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), l.data_ptr(),
+                                    B, H, N, d, scale, causal, dropout_p, seed, _stream(q))
+        else:
+            st = abi.fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), l.data_ptr(),
+                            B, H, N, d, scale, causal, _stream(q))
+    abi.check("fa_fwd_dropout" if dropout_p > 0 else "fa_fwd", st)
     return o, l
 
 
@@ -70,8 +76,9 @@ def workspace_bytes(B: int, H: int, N: int, d: int) -> int:
 
 
 def backward(q, k, v, o, do, lse, causal: bool = False, scale: float | None = None,
-             workspace=None, grads=None):
-    """dQ, dK, dV of attention for upstream gradient `do` (O and LSE from forward)."""
+             workspace=None, grads=None, dropout_p: float = 0.0, seed: int = 0):
+    """dQ, dK, dV of attention for upstream gradient `do` (O and LSE from forward; with
+    dropout, the forward's dropout_p and seed)."""
     _check_qkv(q, k, v, o, do)
     B, H, N, d = q.shape
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
@@ -81,12 +88,16 @@ def backward(q, k, v, o, do, lse, causal: bool = False, scale: float | None = No
     if grads is None:
         grads = (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v))
     dq, dk, dv = grads
+    ptrs = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(),
+            lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr())
     with torch.cuda.device(q.device):
-        st = abi.fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(),
-                        lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
-                        B, H, N, d, scale, causal, workspace.data_ptr(), workspace.numel(),
-                        _stream(q))
-    abi.check("fa_bwd", st)
+        if dropout_p > 0:
+            st = abi.fa_bwd_dropout(*ptrs, B, H, N, d, scale, causal, dropout_p, seed,
+                                    workspace.data_ptr(), workspace.numel(), _stream(q))
+        else:
+            st = abi.fa_bwd(*ptrs, B, H, N, d, scale, causal, workspace.data_ptr(), workspace.numel(),
+                            _stream(q))
+    abi.check("fa_bwd_dropout" if dropout_p > 0 else "fa_bwd", st)
     return dq, dk, dv
 
 

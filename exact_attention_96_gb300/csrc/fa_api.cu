@@ -117,31 +117,22 @@ WsLayout ws_layout(int B, int H, int N, int d) {
   return w;
 }
 
-}  // namespace
 
-extern "C" {
-
-const char* fa_status_string(fa_status s) {
-  switch (s) {
-    case FA_OK: return "FA_OK";
-    case FA_ERR_INVALID_ARG: return "FA_ERR_INVALID_ARG";
-    case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED";
-    case FA_ERR_MISALIGNED: return "FA_ERR_MISALIGNED";
-    case FA_ERR_CUDA: return "FA_ERR_CUDA";
-    case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT";
-  }
-  return "FA_ERR_UNKNOWN";
+// Dropout parameters from the probability and seed: threshold t = round(p * 2^16) (ties to
+// even, at most 2^16 - 1), scale 2^16 / (2^16 - t).
+fa_status make_dropout(double p, unsigned long long seed, fa::DropoutParams* dp) {
+  if (!(p >= 0.0 && p < 1.0)) return FA_ERR_INVALID_ARG;
+  const double t = std::min(std::nearbyint(p * 65536.0), 65535.0);
+  dp->threshold = uint32_t(t);
+  dp->scale = float(65536.0 / (65536.0 - t));
+  dp->seed_lo = uint32_t(seed & 0xFFFFFFFFull);
+  dp->seed_hi = uint32_t(seed >> 32);
+  return FA_OK;
 }
 
-int fa_test_withhold_kv_tile(int tile) { return g_withhold_k_tile.exchange(tile < 0 ? -1 : tile); }
-
-uint64_t fa_set_wait_limit_ns(uint64_t ns) {
-  if (ns < 1000000ull) ns = 1000000ull;
-  return g_wait_limit_ns.exchange(ns);
-}
-
-fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
-                 int d, float scale, int causal, fa_stream_t stream) {
+// Forward of the square problem; `dp` null: no dropout.
+fa_status fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+                   float scale, int causal, const fa::DropoutParams* dp, fa_stream_t stream) {
   if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
   fa_status st = check_sizes(B, H, N, d);
   if (st != FA_OK) return st;
@@ -172,8 +163,106 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
   a.wait_limit_ns = g_wait_limit_ns.load();
   a.err_word = err;
   a.withhold_k_tile = g_withhold_k_tile.exchange(-1);
-  const cudaError_t e = fa::launch_fwd(maps, a, d, causal != 0, reinterpret_cast<cudaStream_t>(stream));
+  a.dropout = dp ? *dp : fa::DropoutParams{0u, 1.f, 0u, 0u};
+  const cudaError_t e =
+      fa::launch_fwd(maps, a, d, causal != 0, reinterpret_cast<cudaStream_t>(stream), dp != nullptr);
   return e == cudaSuccess ? FA_OK : cuda_fail(e);
+}
+
+// Backward; `dp` null: no dropout (with dropout d <= 128).
+fa_status bwd_impl(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                   const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d, float scale,
+                   int causal, const fa::DropoutParams* dp, void* workspace, size_t workspace_bytes,
+                   fa_stream_t stream) {
+  if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv || !workspace) return FA_ERR_INVALID_ARG;
+  fa_status st = check_sizes(B, H, N, d);
+  if (st != FA_OK) return st;
+  if ((st = check_scale(scale)) != FA_OK) return st;
+  const WsLayout w = ws_layout(B, H, N, d);
+  if (workspace_bytes < w.total) return FA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dout) ||
+      !aligned16(lse) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv) ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return FA_ERR_MISALIGNED;
+  int dev = 0;
+  int* err = nullptr;
+  if ((st = device_setup(&dev, &err)) != FA_OK) return st;
+
+  const int BH = B * H;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  fa::BwdMaps maps;
+  CUtensorMap m_lse2, m_dvec, m_dk, m_dv;
+  if (!encode_bf16_rows(&maps.q, q, BH, N, d, 128) || !encode_bf16_rows(&maps.k, k, BH, N, d, 128) ||
+      !encode_bf16_rows(&maps.v, v, BH, N, d, 128) || !encode_bf16_rows(&maps.dout, dout, BH, N, d, 128) ||
+      !encode_bf16_rows(&m_dk, dk, BH, N, d, 128) || !encode_bf16_rows(&m_dv, dv, BH, N, d, 128) ||
+      !encode_f32_rows(&m_lse2, ws + w.lse2_off, BH, w.Np) || !encode_f32_rows(&m_dvec, ws + w.dvec_off, BH, w.Np))
+    return FA_ERR_CUDA;
+  if (d == 256 && (!encode_bf16_rows(&maps.q64, q, BH, N, d, 64) ||
+                   !encode_bf16_rows(&maps.dout64, dout, BH, N, d, 64) ||
+                   !encode_f32_rows(&maps.lse2_64, ws + w.lse2_off, BH, w.Np, 64) ||
+                   !encode_f32_rows(&maps.dvec_64, ws + w.dvec_off, BH, w.Np, 64)))
+    return FA_ERR_CUDA;
+  fa::BwdArgs a;
+  a.q = static_cast<const uint16_t*>(q);
+  a.k = static_cast<const uint16_t*>(k);
+  a.v = static_cast<const uint16_t*>(v);
+  a.o = static_cast<const uint16_t*>(o);
+  a.dout = static_cast<const uint16_t*>(dout);
+  a.lse = lse;
+  a.dq = static_cast<uint16_t*>(dq);
+  a.dk = static_cast<uint16_t*>(dk);
+  a.dv = static_cast<uint16_t*>(dv);
+  a.dvec = reinterpret_cast<float*>(ws + w.dvec_off);
+  a.lse2 = reinterpret_cast<float*>(ws + w.lse2_off);
+  a.dq_acc = reinterpret_cast<float*>(ws + w.dq_off);
+  a.N = N;
+  a.BH = BH;
+  a.d = d;
+  a.scale = scale;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.wait_limit_ns = g_wait_limit_ns.load();
+  a.err_word = err;
+  a.dropout = dp ? *dp : fa::DropoutParams{0u, 1.f, 0u, 0u};
+  const cudaError_t e = fa::launch_bwd_all(maps, m_lse2, m_dvec, m_dk, m_dv, a, causal != 0, w.Np,
+                                           reinterpret_cast<cudaStream_t>(stream), dp != nullptr);
+  return e == cudaSuccess ? FA_OK : cuda_fail(e);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* fa_status_string(fa_status s) {
+  switch (s) {
+    case FA_OK: return "FA_OK";
+    case FA_ERR_INVALID_ARG: return "FA_ERR_INVALID_ARG";
+    case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED";
+    case FA_ERR_MISALIGNED: return "FA_ERR_MISALIGNED";
+    case FA_ERR_CUDA: return "FA_ERR_CUDA";
+    case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT";
+  }
+  return "FA_ERR_UNKNOWN";
+}
+
+int fa_test_withhold_kv_tile(int tile) { return g_withhold_k_tile.exchange(tile < 0 ? -1 : tile); }
+
+uint64_t fa_set_wait_limit_ns(uint64_t ns) {
+  if (ns < 1000000ull) ns = 1000000ull;
+  return g_wait_limit_ns.exchange(ns);
+}
+
+fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
+                 int d, float scale, int causal, fa_stream_t stream) {
+  return fwd_impl(q, k, v, o, lse, B, H, N, d, scale, causal, nullptr, stream);
+}
+
+fa_status fa_fwd_dropout(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
+                         int d, float scale, int causal, double dropout_p, unsigned long long seed,
+                         fa_stream_t stream) {
+  fa::DropoutParams dp;
+  const fa_status st = make_dropout(dropout_p, seed, &dp);
+  if (st != FA_OK) return st;
+  return fwd_impl(q, k, v, o, lse, B, H, N, d, scale, causal, &dp, stream);
 }
 
 namespace {
@@ -318,57 +407,20 @@ size_t fa_bwd_workspace_bytes(int B, int H, int N, int d) {
 fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
                  const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d, float scale,
                  int causal, void* workspace, size_t workspace_bytes, fa_stream_t stream) {
-  if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv || !workspace) return FA_ERR_INVALID_ARG;
-  fa_status st = check_sizes(B, H, N, d);
-  if (st != FA_OK) return st;
-  if ((st = check_scale(scale)) != FA_OK) return st;
-  const WsLayout w = ws_layout(B, H, N, d);
-  if (workspace_bytes < w.total) return FA_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dout) ||
-      !aligned16(lse) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv) ||
-      (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
-    return FA_ERR_MISALIGNED;
-  int dev = 0;
-  int* err = nullptr;
-  if ((st = device_setup(&dev, &err)) != FA_OK) return st;
+  return bwd_impl(q, k, v, o, dout, lse, dq, dk, dv, B, H, N, d, scale, causal, nullptr, workspace,
+                  workspace_bytes, stream);
+}
 
-  const int BH = B * H;
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
-  fa::BwdMaps maps;
-  CUtensorMap m_lse2, m_dvec, m_dk, m_dv;
-  if (!encode_bf16_rows(&maps.q, q, BH, N, d, 128) || !encode_bf16_rows(&maps.k, k, BH, N, d, 128) ||
-      !encode_bf16_rows(&maps.v, v, BH, N, d, 128) || !encode_bf16_rows(&maps.dout, dout, BH, N, d, 128) ||
-      !encode_bf16_rows(&m_dk, dk, BH, N, d, 128) || !encode_bf16_rows(&m_dv, dv, BH, N, d, 128) ||
-      !encode_f32_rows(&m_lse2, ws + w.lse2_off, BH, w.Np) || !encode_f32_rows(&m_dvec, ws + w.dvec_off, BH, w.Np))
-    return FA_ERR_CUDA;
-  if (d == 256 && (!encode_bf16_rows(&maps.q64, q, BH, N, d, 64) ||
-                   !encode_bf16_rows(&maps.dout64, dout, BH, N, d, 64) ||
-                   !encode_f32_rows(&maps.lse2_64, ws + w.lse2_off, BH, w.Np, 64) ||
-                   !encode_f32_rows(&maps.dvec_64, ws + w.dvec_off, BH, w.Np, 64)))
-    return FA_ERR_CUDA;
-  fa::BwdArgs a;
-  a.q = static_cast<const uint16_t*>(q);
-  a.k = static_cast<const uint16_t*>(k);
-  a.v = static_cast<const uint16_t*>(v);
-  a.o = static_cast<const uint16_t*>(o);
-  a.dout = static_cast<const uint16_t*>(dout);
-  a.lse = lse;
-  a.dq = static_cast<uint16_t*>(dq);
-  a.dk = static_cast<uint16_t*>(dk);
-  a.dv = static_cast<uint16_t*>(dv);
-  a.dvec = reinterpret_cast<float*>(ws + w.dvec_off);
-  a.lse2 = reinterpret_cast<float*>(ws + w.lse2_off);
-  a.dq_acc = reinterpret_cast<float*>(ws + w.dq_off);
-  a.N = N;
-  a.BH = BH;
-  a.d = d;
-  a.scale = scale;
-  a.scale_log2 = scale * 1.4426950408889634f;
-  a.wait_limit_ns = g_wait_limit_ns.load();
-  a.err_word = err;
-  const cudaError_t e = fa::launch_bwd_all(maps, m_lse2, m_dvec, m_dk, m_dv, a, causal != 0, w.Np,
-                                           reinterpret_cast<cudaStream_t>(stream));
-  return e == cudaSuccess ? FA_OK : cuda_fail(e);
+fa_status fa_bwd_dropout(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                         const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d, float scale,
+                         int causal, double dropout_p, unsigned long long seed, void* workspace,
+                         size_t workspace_bytes, fa_stream_t stream) {
+  fa::DropoutParams dp;
+  const fa_status st = make_dropout(dropout_p, seed, &dp);
+  if (st != FA_OK) return st;
+  if (d == 256) return FA_ERR_UNSUPPORTED;
+  return bwd_impl(q, k, v, o, dout, lse, dq, dk, dv, B, H, N, d, scale, causal, &dp, workspace,
+                  workspace_bytes, stream);
 }
 
 fa_status fa_status_check(fa_stream_t stream) {

@@ -34,6 +34,15 @@
 // dQ accumulator layout (fp32): [B*H][q tile][d/4][128 rows][4] -- for a fixed group of four
 // columns, the 128 rows of a tile are contiguous, so the 32 lanes of a warp adding one
 // float4 each touch one contiguous 512-byte span.
+//
+// Dropout (template flag, d <= 128; "FlashAttention 与显存" §09: the mask is not stored but
+// regenerated from the generator state): with Z = keep * scale_keep the gradients are
+//   dV = (P * Z)^T dO,  dS = P * (dP * Z - D)   (D = rowsum(dO * O) as before).
+// A key-row thread needs the keep bits of its key for 64 queries.  The eight lanes holding
+// keys 8g .. 8g+7 share the generator calls of those keys: lane u draws the call of query
+// 8b + u (8 bits, one per key), the octet exchanges its 8 bytes by shuffles and each lane
+// takes its own bit column -- one call per lane per 8 queries, made before S^T is waited for.
+// P^T * keep goes to TMEM for the dV product (scale_keep applied to dV at the end).
 
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -191,7 +200,32 @@ struct BwdLayout {
   static_assert(kBytes <= 232448, "shared memory budget");
 };
 
-template <int D, int NS, bool CAUSAL>
+// Keep bits of key `key` for queries qb .. qb+63 (bit c of the result = query qb + c).  All 32
+// lanes of the warp take part (shuffles); lane & 7 must equal key & 7.
+__device__ __forceinline__ uint64_t dropout_key_bits64(const DropoutParams& dp, int key, int qb, int bh, int lane) {
+  const uint32_t u = uint32_t(lane & 7);
+  const uint32_t g = uint32_t(key) >> 3;
+  uint64_t out = 0;
+#pragma unroll
+  for (int b = 0; b < 8; ++b) {
+    // row u of this octet's 8 x 8 bit block: the keep bits of keys 8g .. 8g+7 for query 8b + u
+    const uint32_t row = dropout_keep8(dp, g, uint32_t(qb + 8 * b) + u, uint32_t(bh));
+    uint32_t x = row << (8 * (u & 3));
+    x |= __shfl_xor_sync(0xffffffffu, x, 1);
+    x |= __shfl_xor_sync(0xffffffffu, x, 2);  // rows of this quad of lanes
+    const uint32_t y = __shfl_xor_sync(0xffffffffu, x, 4);
+    const uint32_t lo = u < 4 ? x : y;      // rows 0-3, one per byte
+    const uint32_t hi = u < 4 ? y : x;      // rows 4-7
+    // column u: bit u of every byte, gathered into a nibble (the four products land on
+    // distinct bits 24..27, so no carries)
+    const uint32_t nlo = (((lo >> u) & 0x01010101u) * 0x01020408u) >> 24;
+    const uint32_t nhi = (((hi >> u) & 0x01010101u) * 0x01020408u) >> 24;
+    out |= uint64_t(nlo | (nhi << 4)) << (8 * b);
+  }
+  return out;
+}
+
+template <int D, int NS, bool CAUSAL, bool DROPOUT>
 __global__ void __launch_bounds__(kMainThreads, 1)
 fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
@@ -403,6 +437,15 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
       const bool edge = (CAUSAL && it == 0) || (q0 + kTile > N);  // any masking in this tile
       const float* lse2 = reinterpret_cast<const float*>(smem + L::kLseOff + st * 512) + c0;
       const float* dvv = reinterpret_cast<const float*>(smem + L::kDOff + st * 512) + c0;
+      uint32_t km[2] = {0u, 0u};  // dropout keep bits: bit c % 32 of word c / 32 = query q0 + c0 + c
+      if constexpr (DROPOUT) {
+        const uint64_t bits = dropout_key_bits64(args.dropout, key, q0 + c0, bh, lane);
+        km[0] = uint32_t(bits);
+        km[1] = uint32_t(bits >> 32);
+        // keep the generator work here, ahead of the S^T wait, instead of letting it sink into
+        // the register-heavy conversion below
+        asm volatile("" : "+r"(km[0]), "+r"(km[1]));
+      }
       // phase 1: P^T
       if (!__all_sync(0xffffffffu, mbar_wait(bar(L::kBarSFull), ph, wc))) { ok = false; break; }
       tc_fence_after_sync();
@@ -432,6 +475,13 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
         }
 #pragma unroll
         for (int e = 0; e < 16; ++e) pkeep[cc / 2 + e] = w[e];
+        if constexpr (DROPOUT) {  // the dV product sees P^T * keep
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const uint32_t kb = km[cc / 32] >> (2 * e);
+            w[e] &= ((kb & 1u) ? 0x0000FFFFu : 0u) | ((kb & 2u) ? 0xFFFF0000u : 0u);
+          }
+        }
         tmem_st16(tmem + lane_off + L::kColS + c0 + cc / 2, w);
       }
       tmem_wait_st();
@@ -458,8 +508,14 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
         for (int e = 0; e < 32; e += 2) {
           const float p0 = __uint_as_float(pr[e / 2] << 16);
           const float p1 = __uint_as_float(pr[e / 2] & 0xFFFF0000u);
-          float ds0 = p0 * (__uint_as_float(r[e]) - dl[e]);
-          float ds1 = p1 * (__uint_as_float(r[e + 1]) - dl[e + 1]);
+          float dp0 = __uint_as_float(r[e]), dp1 = __uint_as_float(r[e + 1]);
+          if constexpr (DROPOUT) {
+            const uint32_t kb = km[cc / 32] >> e;
+            dp0 = (kb & 1u) ? dp0 * args.dropout.scale : 0.f;
+            dp1 = (kb & 2u) ? dp1 * args.dropout.scale : 0.f;
+          }
+          float ds0 = p0 * (dp0 - dl[e]);
+          float ds1 = p1 * (dp1 - dl[e + 1]);
           if (edge) {
             const int qa = q0 + c0 + cc + e;
             if (qa >= N) ds0 = 0.f;
@@ -484,7 +540,7 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
     // tile and written by one TMA store per 64-column slab
     const bool fin = ok && __all_sync(0xffffffffu, mbar_wait(bar(L::kBarAccDone), 0, wc));
     const uint32_t col = half == 0 ? L::kColDV : L::kColDK;
-    const float mul = half == 0 ? 1.f : args.scale;
+    const float mul = half == 0 ? (DROPOUT ? args.dropout.scale : 1.f) : args.scale;
     uint8_t* stage = smem + (half == 0 ? L::kQOff : L::kdOOff);
     if (fin) {
       tc_fence_after_sync();
@@ -559,9 +615,10 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
 
 template <int D, int NS, bool CAUSAL>
 cudaError_t launch_main(const BwdMaps& m, const CUtensorMap& lse2, const CUtensorMap& dmap,
-                        const CUtensorMap& dk, const CUtensorMap& dv, const BwdArgs& a, cudaStream_t s) {
+                        const CUtensorMap& dk, const CUtensorMap& dv, const BwdArgs& a, cudaStream_t s,
+                        bool dropout) {
   using L = BwdLayout<D, NS>;
-  auto kern = fa_bwd_main_kernel<D, NS, CAUSAL>;
+  auto kern = dropout ? fa_bwd_main_kernel<D, NS, CAUSAL, true> : fa_bwd_main_kernel<D, NS, CAUSAL, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
   if (e != cudaSuccess) return e;
   dim3 grid((a.N + kTile - 1) / kTile, a.BH);
@@ -591,23 +648,24 @@ cudaError_t launch_prep_and_convert(const BwdArgs& a, int Np, int n_q_tiles, cud
 // (tile order for d <= 128, row-major for d = 256).
 cudaError_t launch_bwd_all(const BwdMaps& m, const CUtensorMap& lse2, const CUtensorMap& dmap,
                            const CUtensorMap& dk, const CUtensorMap& dv, const BwdArgs& a, bool causal,
-                           int Np, cudaStream_t s) {
+                           int Np, cudaStream_t s, bool dropout) {
   const int n_q_tiles = (a.N + kTile - 1) / kTile;
   cudaError_t e;
   switch (a.d) {
     case 64:
       if ((e = launch_prep_and_convert<64>(a, Np, n_q_tiles, s, true)) != cudaSuccess) return e;
-      e = causal ? launch_main<64, 3, true>(m, lse2, dmap, dk, dv, a, s)
-                 : launch_main<64, 3, false>(m, lse2, dmap, dk, dv, a, s);
+      e = causal ? launch_main<64, 3, true>(m, lse2, dmap, dk, dv, a, s, dropout)
+                 : launch_main<64, 3, false>(m, lse2, dmap, dk, dv, a, s, dropout);
       if (e != cudaSuccess) return e;
       return launch_prep_and_convert<64>(a, Np, n_q_tiles, s, false);
     case 128:
       if ((e = launch_prep_and_convert<128>(a, Np, n_q_tiles, s, true)) != cudaSuccess) return e;
-      e = causal ? launch_main<128, 2, true>(m, lse2, dmap, dk, dv, a, s)
-                 : launch_main<128, 2, false>(m, lse2, dmap, dk, dv, a, s);
+      e = causal ? launch_main<128, 2, true>(m, lse2, dmap, dk, dv, a, s, dropout)
+                 : launch_main<128, 2, false>(m, lse2, dmap, dk, dv, a, s, dropout);
       if (e != cudaSuccess) return e;
       return launch_prep_and_convert<128>(a, Np, n_q_tiles, s, false);
     case 256:
+      if (dropout) return cudaErrorNotSupported;
       if ((e = launch_prep_and_convert<256>(a, Np, n_q_tiles, s, true)) != cudaSuccess) return e;
       e = launch_bwd_main_d256(m.q64, m.k, m.v, m.dout64, m.lse2_64, m.dvec_64, dk, dv, a, causal, s);
       if (e != cudaSuccess) return e;

@@ -27,6 +27,13 @@
 //
 // Every wait is bounded (see WaitCtl): on timeout the kernel records the error, skips the
 // rest of the work, waits for its own copies and MMAs to land and frees TMEM.
+//
+// Dropout (template flag; "FlashAttention 与显存" §07: applied inside the fused kernel): a
+// softmax thread draws the keep bits of its row for the coming key tile (one generator call
+// per 8 keys, philox.cuh) before it waits for S, so the integer work overlaps the Q K^T
+// product.  P enters the P V product with dropped entries zeroed; the running sum l and the
+// LSE are those of the undropped P, and the inverse keep probability is folded into the final
+// 1 / l.
 
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -78,7 +85,7 @@ struct FwdLayout {
   static_assert(D % 64 == 0 && BC % 32 == 0 && BC <= 256, "tile shape");
 };
 
-template <int D, int BC, int NS, bool CAUSAL, bool SPLIT>
+template <int D, int BC, int NS, bool CAUSAL, bool SPLIT, bool DROPOUT>
 __global__ void __launch_bounds__(kThreads, 1)
 fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
               const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
@@ -248,6 +255,16 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     bool ok = true;
     for (int j = 0; j < nkv; ++j) {
       const int b = j & 1;
+      const int kv0 = (t_begin + j) * BC;
+      uint32_t km[DROPOUT ? BC / 32 : 1];  // keep bits: bit c % 32 of word c / 32 = key kv0 + c
+      if constexpr (DROPOUT) {
+#pragma unroll
+        for (int w = 0; w < BC / 32; ++w) km[w] = 0u;
+#pragma unroll
+        for (int c = 0; c < BC; c += 8)
+          km[c / 32] |= dropout_keep8(args.dropout, uint32_t((kv0 + c) >> 3), uint32_t(row_g), uint32_t(bh))
+                        << (c % 32);
+      }
       // tcgen05.ld is warp-collective: every wait outcome is made warp-uniform
       if (!__all_sync(0xffffffffu, mbar_wait(bar(L::kBarSFull + b), (j >> 1) & 1, wc))) { ok = false; break; }
       tc_fence_after_sync();
@@ -263,7 +280,6 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       mbar_arrive(bar(L::kBarSFree + b));
 
       // keys kv0 + c are visible for c < lim (sequence tail; causal: key <= query)
-      const int kv0 = (t_begin + j) * BC;
       int lim = Nk - kv0;
       if (CAUSAL) lim = min(lim, row_g - kv0 + 1);
       if (lim < BC) {
@@ -290,7 +306,12 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         const float p1 = ex2_approx(fmaf(s[c + 1], sl2, neg_m));
         sum0 += p0;
         sum1 += p1;
-        pk[c / 2] = pack_bf16x2(p0, p1);
+        if constexpr (DROPOUT) {
+          const uint32_t kb = km[c / 32] >> (c % 32);
+          pk[c / 2] = pack_bf16x2((kb & 1u) ? p0 : 0.f, (kb & 2u) ? p1 : 0.f);
+        } else {
+          pk[c / 2] = pack_bf16x2(p0, p1);
+        }
       }
       l_run = l_run * alpha + (sum0 + sum1);
       // P_j into its TMEM buffer (its previous reader, P_{j-2} V_{j-2}, finished before
@@ -349,7 +370,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       if (row_g < N) args.lse_part[prow] = (m_run + lg2_approx(l_run)) * 0.69314718055994531f;
     } else if (fin) {
       tc_fence_after_sync();
-      const float inv_l = 1.f / l_run;
+      const float inv_l = (DROPOUT ? args.dropout.scale : 1.f) / l_run;
       uint8_t* stage = smem + L::kQOff;  // Q is no longer read by any MMA
 #pragma unroll 1
       for (int c = 0; c < D; c += 32) {
@@ -391,11 +412,14 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
 }
 
 template <int D, int BC, int NS, bool CAUSAL>
-cudaError_t launch_cfg(const Maps& m, const FwdArgs& a, cudaStream_t s) {
+cudaError_t launch_cfg(const Maps& m, const FwdArgs& a, cudaStream_t s, bool dropout) {
   using L = FwdLayout<D, BC, NS>;
-  // split-KV partial outputs are a separate instantiation (non-causal only), so the square
+  // split-KV partial outputs and dropout are separate instantiations, so the plain square
   // problem's kernel carries none of that code
-  auto kern = a.o_part != nullptr ? fa_fwd_kernel<D, BC, NS, CAUSAL, true> : fa_fwd_kernel<D, BC, NS, CAUSAL, false>;
+  if (dropout && a.o_part != nullptr) return cudaErrorInvalidValue;
+  auto kern = dropout ? fa_fwd_kernel<D, BC, NS, CAUSAL, false, true>
+                      : (a.o_part != nullptr ? fa_fwd_kernel<D, BC, NS, CAUSAL, true, false>
+                                             : fa_fwd_kernel<D, BC, NS, CAUSAL, false, false>);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemAlloc);
   if (e != cudaSuccess) return e;
   dim3 grid(a.n_q_tiles, a.BH, a.num_splits);
@@ -407,15 +431,17 @@ cudaError_t launch_cfg(const Maps& m, const FwdArgs& a, cudaStream_t s) {
 
 int fwd_kv_tile(int d) { return d == 128 ? 128 : 64; }
 
-cudaError_t launch_fwd(const Maps& m, const FwdArgs& a, int d, bool causal, cudaStream_t s) {
+cudaError_t launch_fwd(const Maps& m, const FwdArgs& a, int d, bool causal, cudaStream_t s, bool dropout) {
   switch (d) {
     case 64:
       // 64-key tiles keep TMEM at 256 columns and shared memory near 81 KB: two CTAs per SM
-      return causal ? launch_cfg<64, 64, 4, true>(m, a, s) : launch_cfg<64, 64, 4, false>(m, a, s);
+      return causal ? launch_cfg<64, 64, 4, true>(m, a, s, dropout) : launch_cfg<64, 64, 4, false>(m, a, s, dropout);
     case 128:
-      return causal ? launch_cfg<128, 128, 2, true>(m, a, s) : launch_cfg<128, 128, 2, false>(m, a, s);
+      return causal ? launch_cfg<128, 128, 2, true>(m, a, s, dropout)
+                    : launch_cfg<128, 128, 2, false>(m, a, s, dropout);
     case 256:
-      return causal ? launch_cfg<256, 64, 2, true>(m, a, s) : launch_cfg<256, 64, 2, false>(m, a, s);
+      return causal ? launch_cfg<256, 64, 2, true>(m, a, s, dropout)
+                    : launch_cfg<256, 64, 2, false>(m, a, s, dropout);
     default:
       return cudaErrorInvalidValue;
   }

@@ -7,6 +7,8 @@
 #include <cstddef>
 #include <cstdint>
 
+#include "philox.cuh"
+
 namespace fa {
 
 // Everything a forward launch needs besides the four tensor maps.
@@ -24,6 +26,7 @@ struct FwdArgs {
   uint64_t wait_limit_ns;
   int* err_word;        // per-device error word
   int withhold_k_tile;  // test hook: the producer never loads this K tile (-1: none)
+  DropoutParams dropout;  // used by the dropout instantiation only
 };
 
 // Tensor maps of one [B*H, N, d] bf16 tensor: `rows128` boxes of 64 columns x 128 rows,
@@ -32,8 +35,10 @@ struct Maps {
   CUtensorMap q, k, v, o;
 };
 
-// Forward: one launch.  Returns the cudaError_t of the launch.
-cudaError_t launch_fwd(const Maps& maps, const FwdArgs& a, int d, bool causal, cudaStream_t s);
+// Forward: one launch.  Returns the cudaError_t of the launch.  With `dropout` the kernel
+// applies the mask of a.dropout (square problem only: no split mode).
+cudaError_t launch_fwd(const Maps& maps, const FwdArgs& a, int d, bool causal, cudaStream_t s,
+                       bool dropout = false);
 // Key-tile height the forward kernel uses for head dim d (the K/V tensor-map box height).
 int fwd_kv_tile(int d);
 
@@ -62,6 +67,7 @@ struct BwdArgs {
   float scale_log2;
   uint64_t wait_limit_ns;
   int* err_word;
+  DropoutParams dropout;  // threshold 0 with scale 1: no dropout
 };
 
 struct BwdMaps {
@@ -79,8 +85,9 @@ cudaError_t launch_bwd_main_d256(const CUtensorMap& q64, const CUtensorMap& k, c
 // Backward: prep, main and dQ-convert launches.  `lse2` and `dvec` describe the fp32
 // [B*H, Np] rows of the workspace (box 128 x 1 x 1); `dk`, `dv` the bf16 outputs.
 // Np = N rounded up to a multiple of 4.
+// With `dropout` (d <= 128 only) the main kernel applies the mask of a.dropout.
 cudaError_t launch_bwd_all(const BwdMaps& m, const CUtensorMap& lse2, const CUtensorMap& dvec,
                            const CUtensorMap& dk, const CUtensorMap& dv, const BwdArgs& a,
-                           bool causal, int Np, cudaStream_t s);
+                           bool causal, int Np, cudaStream_t s, bool dropout = false);
 
 }  // namespace fa

@@ -123,6 +123,31 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
                  void* workspace, size_t workspace_bytes, fa_stream_t stream);
 
 /*
+ * Dropout ("FlashAttention 与显存" §07: applied inside the fused kernel; §09: the mask is not
+ * stored, the backward pass regenerates it from the generator state).  After the softmax each
+ * probability P_ij is multiplied by Z_ij = keep_ij / q_keep:
+ *     O = (P * Z) V,  LSE unchanged (that of the undropped P),
+ *     dV = (P * Z)^T dO,  dS = P * (dP * Z - D),  D = rowsum(dO * O).
+ * The mask is a pure function of (seed, head index bh = b*H + h, query i, key j): the 16-bit
+ * half j % 2 (0 = low) of word (j % 8) / 2 of Philox4x32-10 (Salmon et al., SC 2011) with
+ * counter (j / 8, i, bh, 0) and key (seed & 0xffffffff, seed >> 32); keep_ij = (half >= t),
+ * t = round(dropout_p * 2^16) (ties to even, at most 2^16 - 1), q_keep = (2^16 - t) / 2^16.
+ * So dropout_p is quantised to multiples of 2^-16 and E[Z] = 1 exactly.
+ *   dropout_p: in [0, 1), else FA_ERR_INVALID_ARG.  seed: any 64-bit value.
+ * fa_fwd_dropout takes fa_fwd's arguments plus (dropout_p, seed); fa_bwd_dropout takes
+ * fa_bwd's plus the same pair, which must be those of the forward call (with lse and o from
+ * it).  fa_bwd_dropout with d = 256 returns FA_ERR_UNSUPPORTED.
+ */
+fa_status fa_fwd_dropout(const void* q, const void* k, const void* v, void* o, float* lse,
+                         int B, int H, int N, int d, float scale, int causal,
+                         double dropout_p, unsigned long long seed, fa_stream_t stream);
+fa_status fa_bwd_dropout(const void* q, const void* k, const void* v, const void* o,
+                         const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                         int B, int H, int N, int d, float scale, int causal,
+                         double dropout_p, unsigned long long seed,
+                         void* workspace, size_t workspace_bytes, fa_stream_t stream);
+
+/*
  * Size in bytes of the static scratch array used by fa_bwd_noalloc (64 MiB per device).
  */
 #define FA_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)

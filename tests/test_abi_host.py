@@ -129,3 +129,26 @@ def test_split_plan(lib):
     ws = abi.fa_fwd_splitkv_workspace_bytes(2, 3, 5, 1000, 64, 4)
     rows = 2 * 3 * 5
     assert ws == (4 * rows * 64 * 4 + 255) // 256 * 256 + 4 * rows * 4
+
+
+@pytest.mark.parametrize("p", [1.0, 1.5, -0.1, float("nan"), float("inf")])
+def test_dropout_probability_is_validated(lib, p):
+    assert abi.fa_fwd_dropout(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 128, 64, 0.125, 0, p, 1, None) == \
+        abi.FA_ERR_INVALID_ARG
+    assert abi.fa_bwd_dropout(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 128, 64, 0.125, 0,
+                              p, 1, FAKE, 1 << 30, None) == abi.FA_ERR_INVALID_ARG
+
+
+def test_dropout_argument_checks_before_launch(lib):
+    # the backward dropout path exists for d <= 128 only
+    assert abi.fa_bwd_dropout(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 128, 256, 0.125, 0,
+                              0.1, 1, FAKE, 1 << 30, None) == abi.FA_ERR_UNSUPPORTED
+    # the usual size, pointer and alignment checks still come first
+    assert abi.fa_fwd_dropout(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 0, 64, 0.125, 0, 0.1, 1, None) == \
+        abi.FA_ERR_INVALID_ARG
+    assert abi.fa_fwd_dropout(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 128, 96, 0.125, 0, 0.1, 1, None) == \
+        abi.FA_ERR_UNSUPPORTED
+    assert abi.fa_fwd_dropout(FAKE + 8, FAKE, FAKE, FAKE, FAKE, 1, 1, 128, 64, 0.125, 0, 0.1, 1, None) == \
+        abi.FA_ERR_MISALIGNED
+    assert abi.fa_bwd_dropout(0, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 128, 64, 0.125, 0,
+                              0.1, 1, FAKE, 1 << 30, None) == abi.FA_ERR_INVALID_ARG
