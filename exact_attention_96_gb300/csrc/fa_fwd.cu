@@ -48,7 +48,7 @@ constexpr int kBM = 128;            // query rows per CTA (= TMEM lanes)
 constexpr int kSoftmaxThreads = 128;
 constexpr int kThreads = 192;       // 4 softmax warps + producer warp + MMA warp
 
-template <int D, int BC, int NS>
+template <int D, int BC, int NS, bool DROP = false>
 struct FwdLayout {
   static constexpr int kSlabs = D / 64;
   static constexpr int kQBytes = kBM * D * 2;
@@ -56,7 +56,10 @@ struct FwdLayout {
   static constexpr int kQOff = 0;
   static constexpr int kKOff = kQBytes;
   static constexpr int kVOff = kKOff + NS * kKVBytes;
-  static constexpr int kBarOff = kVOff + NS * kKVBytes;
+  // dropout: the generator words of the current key tile, [BC/8 groups][128 rows] x 16 bytes
+  static constexpr int kDropOff = kVOff + NS * kKVBytes;
+  static constexpr int kDropBytes = DROP ? (BC / 8) * kBM * 16 : 0;
+  static constexpr int kBarOff = kDropOff + kDropBytes;
   // barrier slots
   static constexpr int kBarQFull = 0;
   static constexpr int kBarKFull = 1;
@@ -90,7 +93,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
               const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
               const FwdArgs args) {
-  using L = FwdLayout<D, BC, NS>;
+  using L = FwdLayout<D, BC, NS, DROPOUT>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_addr(smem_raw);
   const uint32_t base = (raw_addr + 1023u) & ~1023u;
@@ -256,14 +259,19 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     for (int j = 0; j < nkv; ++j) {
       const int b = j & 1;
       const int kv0 = (t_begin + j) * BC;
-      uint32_t km[DROPOUT ? BC / 32 : 1];  // keep bits: bit c % 32 of word c / 32 = key kv0 + c
       if constexpr (DROPOUT) {
+        // The generator words of this row for the tile go to shared memory (the row's own
+        // slots: no other thread reads them).  Four calls per iteration, interleaved; the loop
+        // stays rolled, since unrolled the generator code overflows the instruction cache next
+        // to the unrolled softmax.
+        uint4* words = reinterpret_cast<uint4*>(smem + L::kDropOff) + row;
+#pragma unroll 1
+        for (int g = 0; g < BC / 8; g += 4) {
 #pragma unroll
-        for (int w = 0; w < BC / 32; ++w) km[w] = 0u;
-#pragma unroll
-        for (int c = 0; c < BC; c += 8)
-          km[c / 32] |= dropout_keep8(args.dropout, uint32_t((kv0 + c) >> 3), uint32_t(row_g), uint32_t(bh))
-                        << (c % 32);
+          for (int u = 0; u < 4; ++u)
+            words[(g + u) * kBM] =
+                dropout_words(args.dropout, uint32_t((kv0 >> 3) + g + u), uint32_t(row_g), uint32_t(bh));
+        }
       }
       // tcgen05.ld is warp-collective: every wait outcome is made warp-uniform
       if (!__all_sync(0xffffffffu, mbar_wait(bar(L::kBarSFull + b), (j >> 1) & 1, wc))) { ok = false; break; }
@@ -300,6 +308,8 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       const float neg_m = -m_new;
       float sum0 = 0.f, sum1 = 0.f;
       uint32_t pk[BC / 2];
+      [[maybe_unused]] uint4 dw;  // dropout: words of keys c .. c+7
+      [[maybe_unused]] const uint32_t t_lo = args.dropout.threshold, t_hi = args.dropout.threshold << 16;
 #pragma unroll
       for (int c = 0; c < BC; c += 2) {
         const float p0 = ex2_approx(fmaf(s[c], sl2, neg_m));
@@ -307,8 +317,11 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         sum0 += p0;
         sum1 += p1;
         if constexpr (DROPOUT) {
-          const uint32_t kb = km[c / 32] >> (c % 32);
-          pk[c / 2] = pack_bf16x2((kb & 1u) ? p0 : 0.f, (kb & 2u) ? p1 : 0.f);
+          // key c (even) is the low half of its word, key c + 1 the high half; the undropped
+          // values stay in the sums
+          if (c % 8 == 0) dw = reinterpret_cast<const uint4*>(smem + L::kDropOff)[(c / 8) * kBM + row];
+          const uint32_t w = (c % 8 == 0) ? dw.x : (c % 8 == 2) ? dw.y : (c % 8 == 4) ? dw.z : dw.w;
+          pk[c / 2] = pack_bf16x2((w & 0xFFFFu) >= t_lo ? p0 : 0.f, w >= t_hi ? p1 : 0.f);
         } else {
           pk[c / 2] = pack_bf16x2(p0, p1);
         }
@@ -413,17 +426,17 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
 
 template <int D, int BC, int NS, bool CAUSAL>
 cudaError_t launch_cfg(const Maps& m, const FwdArgs& a, cudaStream_t s, bool dropout) {
-  using L = FwdLayout<D, BC, NS>;
+  const int smem = dropout ? FwdLayout<D, BC, NS, true>::kSmemAlloc : FwdLayout<D, BC, NS, false>::kSmemAlloc;
   // split-KV partial outputs and dropout are separate instantiations, so the plain square
   // problem's kernel carries none of that code
   if (dropout && a.o_part != nullptr) return cudaErrorInvalidValue;
   auto kern = dropout ? fa_fwd_kernel<D, BC, NS, CAUSAL, false, true>
                       : (a.o_part != nullptr ? fa_fwd_kernel<D, BC, NS, CAUSAL, true, false>
                                              : fa_fwd_kernel<D, BC, NS, CAUSAL, false, false>);
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemAlloc);
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   dim3 grid(a.n_q_tiles, a.BH, a.num_splits);
-  kern<<<grid, kThreads, L::kSmemAlloc, s>>>(m.q, m.k, m.v, m.o, a);
+  kern<<<grid, kThreads, smem, s>>>(m.q, m.k, m.v, m.o, a);
   return cudaGetLastError();
 }
 

@@ -27,16 +27,22 @@ __device__ __forceinline__ uint4 philox4x32_10(uint32_t c0, uint32_t c1, uint32_
                                                uint32_t k0, uint32_t k1) {
 #pragma unroll
   for (int r = 0; r < 10; ++r) {
-    const uint32_t hi0 = __umulhi(0xD2511F53u, c0), lo0 = 0xD2511F53u * c0;
-    const uint32_t hi1 = __umulhi(0xCD9E8D57u, c2), lo1 = 0xCD9E8D57u * c2;
-    c0 = hi1 ^ c1 ^ k0;
-    c1 = lo1;
-    c2 = hi0 ^ c3 ^ k1;
-    c3 = lo0;
+    const uint64_t p0 = uint64_t(c0) * 0xD2511F53u;  // one 32 x 32 -> 64-bit product each
+    const uint64_t p1 = uint64_t(c2) * 0xCD9E8D57u;
+    c0 = uint32_t(p1 >> 32) ^ c1 ^ k0;
+    c1 = uint32_t(p1);
+    c2 = uint32_t(p0 >> 32) ^ c3 ^ k1;
+    c3 = uint32_t(p0);
     k0 += 0x9E3779B9u;
     k1 += 0xBB67AE85u;
   }
   return make_uint4(c0, c1, c2, c3);
+}
+
+// The four words behind keys 8g .. 8g+7 of query i: word m holds key 8g + 2m in its low
+// half and key 8g + 2m + 1 in its high half.
+__device__ __forceinline__ uint4 dropout_words(const DropoutParams& dp, uint32_t g, uint32_t i, uint32_t bh) {
+  return philox4x32_10(g, i, bh, 0u, dp.seed_lo, dp.seed_hi);
 }
 
 // Keep bits of keys 8g .. 8g+7 (bit u = key 8g + u) for query i of head bh.
