@@ -17,6 +17,10 @@ Philox(counter = (j // 8, i, bh, 0), key = (seed & 0xffffffff, seed >> 32)).  Th
 kept when that half is >= t = min(round(p * 2^16), 2^16 - 1), i.e. with probability
 (2^16 - t) / 2^16, and kept elements are scaled by the inverse of that probability, so the
 mask's expectation is exactly 1 (p is quantised to multiples of 2^-16).
+
+Parity unpinned: the identity of ``philox4x32_10`` with the published generator (no
+known-answer vectors are reproduced here).  What the method needs from the mask -- keep rate,
+uniform draws, dependence on every coordinate, unbiasedness -- is pinned by the tests.
 """
 
 from __future__ import annotations
