@@ -110,7 +110,7 @@ class ClockSampler:
 
 # --------------------------------------------------------------- CPU oracle ----
 
-def cpu_oracle_sample(target_s: float = 12.0, max_heads: int = 4):
+def cpu_oracle_sample(target_s: float = 12.0, max_heads: int = 16):
     """Times the fp64 oracle (forward + backward of whole heads of the workload) until about
     `target_s` seconds of CPU work; returns TFLOP/s under the same FLOP convention."""
     from exact_attention_96_gb300 import inputs as I
