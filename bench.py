@@ -294,6 +294,30 @@ SWEEP_DECODE = [  # (name, B, H, Nq, Nk, d): split-KV forward, HBM-bound (K, V r
 ]
 
 
+SWEEP_FP8 = [  # (name, B, H, N, causal): FP8 forward, head dim 128, seeded E4M3 inputs
+    ("C4-fp8", 4, 16, 8192, True),
+    ("fp8-2x16x8192", 2, 16, 8192, False),
+]
+SWEEP_DROPOUT = [  # (name, B, H, N, d, causal, p): forward and backward with dropout
+    ("C4-dropout", 4, 16, 8192, 128, True, 0.1),
+    ("C3-4096-dropout", 16, 8, 4096, 64, False, 0.1),
+]
+
+
+def timed(fn, reps):
+    import torch
+    for _ in range(3):
+        fn()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        fn()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / reps
+
+
 def naive_peak_bytes(q, k, v, do, scale):
     """Peak extra device memory of standard attention in PyTorch eager (S and P materialised
     in HBM, backward through autograd) -- the comparison the memory experiment makes."""
@@ -372,6 +396,42 @@ def run_sweep(reps: int = 20):
                               "peak_extra_MB_naive_eager": naive / 2**20,
                               "note": "extra device memory beyond q, k, v, dO for one fwd+bwd"}), flush=True)
         del q, k, v, do
+        torch.cuda.empty_cache()
+    for name, B, H, N, causal in SWEEP_FP8:
+        q8, k8, v8, (qs, ks, vs) = I.fp8_attention_inputs(B, H, N, 128, seed=7)
+        ldv = (N + 15) // 16 * 16
+        vt = np.zeros((B, H, 128, ldv), np.uint8)
+        vt[..., :N] = np.swapaxes(v8, -1, -2)
+        tq, tk, tvt = (torch.from_numpy(np.ascontiguousarray(x)).cuda() for x in (q8, k8, vt))
+        o, lse = fa.forward_fp8(tq, tk, tvt, qs, ks, vs, causal=causal)
+        ms = timed(lambda: fa.forward_fp8(tq, tk, tvt, qs, ks, vs, causal=causal, out=o, lse=lse), reps)
+        tf = step_flops(B, H, N, 128, causal)[0] / (ms * 1e-3) / 1e12
+        # the FP8 peak: the measured bf16 peak times the nominal FP8 / bf16 ratio of 2
+        print(json.dumps({"config": name, "shape": [B, H, N, 128], "causal": causal, "pass": "fwd-fp8",
+                          "ms": ms, "tflops": tf, "frac_fp8_sustained": tf / (2 * sustained),
+                          "frac_bf16_sustained": tf / sustained, "peak_source": src}), flush=True)
+        if fa.status_check() != abi.FA_OK:
+            raise RuntimeError(f"device status not OK after {name}")
+        del tq, tk, tvt, o, lse
+        torch.cuda.empty_cache()
+    for name, B, H, N, d, causal, p in SWEEP_DROPOUT:
+        host = I.attention_inputs(B, H, N, d, seed=7, multiplier=0.5 if causal else 1.0)
+        q, k, v, do = (torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).cuda() for x in host)
+        fwd_f, bwd_f = step_flops(B, H, N, d, causal)
+        o, lse = fa.forward(q, k, v, causal=causal, dropout_p=p, seed=1)
+        ws = torch.empty(fa.workspace_bytes(B, H, N, d), dtype=torch.uint8, device="cuda")
+        grads = tuple(torch.empty_like(q) for _ in range(3))
+        ms_f = timed(lambda: fa.forward(q, k, v, causal=causal, out=o, lse=lse, dropout_p=p, seed=1), reps)
+        ms_b = timed(lambda: fa.backward(q, k, v, o, do, lse, causal=causal, workspace=ws, grads=grads,
+                                         dropout_p=p, seed=1), reps)
+        for ps, ms, fl in (("fwd-dropout", ms_f, fwd_f), ("bwd-dropout", ms_b, bwd_f)):
+            tf = fl / (ms * 1e-3) / 1e12
+            print(json.dumps({"config": name, "shape": [B, H, N, d], "causal": causal, "dropout_p": p,
+                              "pass": ps, "ms": ms, "tflops": tf, "frac_sustained": tf / sustained,
+                              "peak_source": src}), flush=True)
+        if fa.status_check() != abi.FA_OK:
+            raise RuntimeError(f"device status not OK after {name}")
+        del q, k, v, do, o, lse, ws, grads
         torch.cuda.empty_cache()
     hbm = peaks["hbm_gbs"]
     for name, B, H, Nq, Nk, d in SWEEP_DECODE:

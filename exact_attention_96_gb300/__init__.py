@@ -6,4 +6,5 @@ points one to one, ``attention`` wraps them for torch tensors, ``inputs`` draws 
 synthetic inputs, ``build`` compiles the library in-tree.
 """
 
-from .attention import forward, forward_splitkv, backward, workspace_bytes, status_check  # noqa: F401
+from .attention import (forward, forward_fp8, forward_splitkv, backward, workspace_bytes,  # noqa: F401
+                        status_check)

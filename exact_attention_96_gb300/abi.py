@@ -27,6 +27,9 @@ _c_size_t = ctypes.c_size_t
 SIGNATURES = {
     "fa_fwd": (_c_int, [_c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_void_p,
                         _c_int, _c_int, _c_int, _c_int, _c_float, _c_int, _c_void_p]),
+    "fa_fwd_fp8": (_c_int, [_c_void_p, _c_void_p, _c_void_p, _c_int, _c_void_p, _c_void_p,
+                            _c_int, _c_int, _c_int, _c_int, _c_float, _c_float, _c_float, _c_float,
+                            _c_int, _c_void_p]),
     "fa_fwd_splitkv_workspace_bytes": (_c_size_t, [_c_int] * 6),
     "fa_fwd_splitkv_num_splits": (_c_int, [_c_int] * 6),
     "fa_fwd_splitkv": (_c_int, [_c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_void_p,
@@ -95,6 +98,12 @@ def check(fn: str, status: int) -> None:
 
 def fa_fwd(q, k, v, o, lse, B, H, N, d, scale, causal, stream) -> int:
     return load().fa_fwd(q, k, v, o, lse, B, H, N, d, scale, int(causal), stream)
+
+
+def fa_fwd_fp8(q8, k8, vt8, ldv, o, lse, B, H, N, d, scale, q_descale, k_descale, v_descale, causal,
+               stream) -> int:
+    return load().fa_fwd_fp8(q8, k8, vt8, ldv, o, lse, B, H, N, d, scale, q_descale, k_descale,
+                             v_descale, int(causal), stream)
 
 
 def fa_fwd_splitkv_workspace_bytes(B, H, Nq, Nk, d, num_splits) -> int:

@@ -47,6 +47,28 @@ def forward(q, k, v, causal: bool = False, scale: float | None = None, out=None,
     return o, l
 
 
+def forward_fp8(q8, k8, vt8, q_descale: float, k_descale: float, v_descale: float,
+                causal: bool = False, scale: float | None = None, out=None, lse=None):
+    """FP8 forward, head dim 128: q8, k8 uint8 E4M3 codes [B, H, N, 128]; vt8 the codes of V
+    transposed, uint8 [B, H, 128, ldv] with ldv >= N a multiple of 16.  Returns bf16 O and
+    fp32 LSE of attention over the real inputs descale * code."""
+    for t in (q8, k8, vt8):
+        if not t.is_cuda or t.dtype != torch.uint8 or not t.is_contiguous() or t.dim() != 4:
+            raise ValueError("expected contiguous uint8 CUDA tensors of rank 4")
+    B, H, N, d = q8.shape
+    if k8.shape != q8.shape or vt8.shape[:3] != (B, H, d):
+        raise ValueError("k8 must match q8; vt8 must be [B, H, d, ldv]")
+    ldv = vt8.shape[3]
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    o = torch.empty((B, H, N, d), dtype=torch.bfloat16, device=q8.device) if out is None else out
+    l = torch.empty((B, H, N), dtype=torch.float32, device=q8.device) if lse is None else lse
+    with torch.cuda.device(q8.device):
+        st = abi.fa_fwd_fp8(q8.data_ptr(), k8.data_ptr(), vt8.data_ptr(), ldv, o.data_ptr(), l.data_ptr(),
+                            B, H, N, d, scale, q_descale, k_descale, v_descale, causal, _stream(q8))
+    abi.check("fa_fwd_fp8", st)
+    return o, l
+
+
 def forward_splitkv(q, k, v, num_splits: int = 0, scale: float | None = None, out=None, lse=None,
                     workspace=None):
     """Split-KV forward (no mask): q [B,H,Nq,d] against k, v [B,H,Nk,d]; returns (O, LSE)."""

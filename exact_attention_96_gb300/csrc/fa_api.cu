@@ -87,6 +87,18 @@ bool encode_bf16_rows(CUtensorMap* m, const void* p, int BH, int N, int d, int r
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// [BH, rows, cols] bytes (E4M3), box (128 columns, 128 rows, 1), 128-byte swizzle.  `ld` is
+// the row stride in bytes (a multiple of 16, >= cols).
+bool encode_u8_rows(CUtensorMap* m, const void* p, int BH, int rows, int cols, int ld) {
+  const cuuint64_t dims[3] = {cuuint64_t(cols), cuuint64_t(rows), cuuint64_t(BH)};
+  const cuuint64_t strides[2] = {cuuint64_t(ld), cuuint64_t(ld) * rows};
+  const cuuint32_t box[3] = {128, 128, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(p), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // [1, BH, Np] fp32 rows, box (box, 1, 1), no swizzle.
 bool encode_f32_rows(CUtensorMap* m, const void* p, int BH, int Np, int box_len = 128) {
   const cuuint64_t dims[3] = {cuuint64_t(Np), cuuint64_t(BH), 1};
@@ -164,6 +176,7 @@ fa_status fwd_impl(const void* q, const void* k, const void* v, void* o, float* 
   a.err_word = err;
   a.withhold_k_tile = g_withhold_k_tile.exchange(-1);
   a.dropout = dp ? *dp : fa::DropoutParams{0u, 1.f, 0u, 0u};
+  a.o_scale = 1.f;
   const cudaError_t e =
       fa::launch_fwd(maps, a, d, causal != 0, reinterpret_cast<cudaStream_t>(stream), dp != nullptr);
   return e == cudaSuccess ? FA_OK : cuda_fail(e);
@@ -340,6 +353,7 @@ fa_status fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, f
   a.wait_limit_ns = g_wait_limit_ns.load();
   a.err_word = err;
   a.withhold_k_tile = -1;
+  a.o_scale = 1.f;
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = fa::launch_fwd(maps, a, d, false, s);
   if (e != cudaSuccess) return cuda_fail(e);
@@ -381,6 +395,7 @@ fa_status fa_fwd_partial(const void* q, const void* k, const void* v, float* o_p
   a.wait_limit_ns = g_wait_limit_ns.load();
   a.err_word = err;
   a.withhold_k_tile = -1;
+  a.o_scale = 1.f;
   const cudaError_t e = fa::launch_fwd(maps, a, d, causal != 0, reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FA_OK : cuda_fail(e);
 }
@@ -421,6 +436,47 @@ fa_status fa_bwd_dropout(const void* q, const void* k, const void* v, const void
   if (d == 256) return FA_ERR_UNSUPPORTED;
   return bwd_impl(q, k, v, o, dout, lse, dq, dk, dv, B, H, N, d, scale, causal, &dp, workspace,
                   workspace_bytes, stream);
+}
+
+fa_status fa_fwd_fp8(const void* q8, const void* k8, const void* vt8, int ldv, void* o, float* lse, int B,
+                     int H, int N, int d, float scale, float q_descale, float k_descale, float v_descale,
+                     int causal, fa_stream_t stream) {
+  if (!q8 || !k8 || !vt8 || !o || !lse) return FA_ERR_INVALID_ARG;
+  fa_status st = check_sizes(B, H, N, d);
+  if (st != FA_OK) return st;
+  if (d != 128) return FA_ERR_UNSUPPORTED;
+  if ((st = check_scale(scale)) != FA_OK || (st = check_scale(q_descale)) != FA_OK ||
+      (st = check_scale(k_descale)) != FA_OK || (st = check_scale(v_descale)) != FA_OK)
+    return st;
+  if (ldv < N || ldv % 16 != 0) return FA_ERR_INVALID_ARG;
+  if (!aligned16(q8) || !aligned16(k8) || !aligned16(vt8) || !aligned16(o) || !aligned16(lse))
+    return FA_ERR_MISALIGNED;
+  int dev = 0;
+  int* err = nullptr;
+  if ((st = device_setup(&dev, &err)) != FA_OK) return st;
+  const int BH = B * H;
+  fa::Maps maps;
+  if (!encode_u8_rows(&maps.q, q8, BH, N, d, d) || !encode_u8_rows(&maps.k, k8, BH, N, d, d) ||
+      !encode_u8_rows(&maps.v, vt8, BH, d, N, ldv) || !encode_bf16_rows(&maps.o, o, BH, N, d, 128))
+    return FA_ERR_CUDA;
+  fa::FwdArgs a;
+  a.lse = lse;
+  a.N = N;
+  a.Nk = N;
+  a.num_splits = 1;
+  a.tiles_per_split = (N + 127) / 128;
+  a.o_part = nullptr;
+  a.lse_part = nullptr;
+  a.BH = BH;
+  a.n_q_tiles = (N + 127) / 128;
+  a.scale_log2 = float(double(scale) * q_descale * k_descale * 1.4426950408889634);
+  a.wait_limit_ns = g_wait_limit_ns.load();
+  a.err_word = err;
+  a.withhold_k_tile = -1;
+  a.dropout = fa::DropoutParams{0u, 1.f, 0u, 0u};
+  a.o_scale = v_descale;
+  const cudaError_t e = fa::launch_fwd_fp8(maps, a, causal != 0, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : cuda_fail(e);
 }
 
 fa_status fa_status_check(fa_stream_t stream) {

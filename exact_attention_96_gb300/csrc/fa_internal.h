@@ -27,6 +27,7 @@ struct FwdArgs {
   int* err_word;        // per-device error word
   int withhold_k_tile;  // test hook: the producer never loads this K tile (-1: none)
   DropoutParams dropout;  // used by the dropout instantiation only
+  float o_scale;          // final output multiplier (FP8: V's descale factor; else 1)
 };
 
 // Tensor maps of one [B*H, N, d] bf16 tensor: `rows128` boxes of 64 columns x 128 rows,
@@ -39,6 +40,9 @@ struct Maps {
 // applies the mask of a.dropout (square problem only: no split mode).
 cudaError_t launch_fwd(const Maps& maps, const FwdArgs& a, int d, bool causal, cudaStream_t s,
                        bool dropout = false);
+// FP8 forward for head dim 128, two query tiles per CTA (fa_fwd_fp8.cu): maps of E4M3 Q, K
+// and of V transposed ([B*H, 128, ldv]), bf16 O.
+cudaError_t launch_fwd_fp8(const Maps& maps, const FwdArgs& a, bool causal, cudaStream_t s);
 // Key-tile height the forward kernel uses for head dim d (the K/V tensor-map box height).
 int fwd_kv_tile(int d);
 

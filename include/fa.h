@@ -62,6 +62,22 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
                  int B, int H, int N, int d, float scale, int causal, fa_stream_t stream);
 
 /*
+ * FP8 forward ("Flash Attention 原理与实践" §3.2: the third version's FP8 mode), head dim 128.
+ *   q8, k8: E4M3 codes [B,H,N,128] (OCP 8-bit floating point, E4M3 variant), one byte each.
+ *   vt8: E4M3 codes of V transposed, [B,H,128,ldv]: element (b,h,c,j) is V[b,h,j,c]; ldv >= N
+ *        and a multiple of 16 (columns j >= N are never read).
+ *   q_descale, k_descale, v_descale: the real inputs are descale * code (finite, > 0).
+ *   o: bf16 [B,H,N,128]; lse: fp32 [B,H,N] -- as fa_fwd for the real inputs.
+ * Both products run on 8-bit operands (tcgen05.mma kind::f8f6f4); P is rounded to E4M3 after
+ * scaling by 2^8, so O carries an error of up to about 2^-4 of max|V| (the rounding of P);
+ * LSE is as accurate as fa_fwd's.  d != 128 -> FA_ERR_UNSUPPORTED; ldv < N or not a multiple
+ * of 16 -> FA_ERR_INVALID_ARG; other errors as for fa_fwd.
+ */
+fa_status fa_fwd_fp8(const void* q8, const void* k8, const void* vt8, int ldv, void* o, float* lse,
+                     int B, int H, int N, int d, float scale, float q_descale, float k_descale,
+                     float v_descale, int causal, fa_stream_t stream);
+
+/*
  * Split-KV forward ("Flash Attention 原理与实践" §5.1, the decoding variant): queries attend to
  * a key/value sequence of a different length, split into key ranges processed by separate
  * CTAs; each range writes its partial output (normalised within the range) and partial

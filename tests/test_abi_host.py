@@ -152,3 +152,20 @@ def test_dropout_argument_checks_before_launch(lib):
         abi.FA_ERR_MISALIGNED
     assert abi.fa_bwd_dropout(0, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 128, 64, 0.125, 0,
                               0.1, 1, FAKE, 1 << 30, None) == abi.FA_ERR_INVALID_ARG
+
+
+def test_fp8_forward_argument_checks_before_launch(lib):
+    def call(**kw):
+        a = dict(q8=FAKE, k8=FAKE, vt8=FAKE, ldv=128, o=FAKE, lse=FAKE, B=1, H=1, N=128, d=128,
+                 scale=0.125, qd=1.0, kd=1.0, vd=1.0, causal=0, stream=None)
+        a.update(kw)
+        return abi.fa_fwd_fp8(*a.values())
+    assert call(d=64) == abi.FA_ERR_UNSUPPORTED
+    assert call(d=256) == abi.FA_ERR_UNSUPPORTED
+    assert call(ldv=112) == abi.FA_ERR_INVALID_ARG        # ldv < N
+    assert call(N=100, ldv=104) == abi.FA_ERR_INVALID_ARG  # not a multiple of 16
+    assert call(qd=0.0) == abi.FA_ERR_INVALID_ARG
+    assert call(vd=float("nan")) == abi.FA_ERR_INVALID_ARG
+    assert call(q8=0) == abi.FA_ERR_INVALID_ARG
+    assert call(vt8=FAKE + 8) == abi.FA_ERR_MISALIGNED
+    assert call(N=0) == abi.FA_ERR_INVALID_ARG
