@@ -116,17 +116,21 @@ def attention_fwd(q, k, v, scale: float, causal: bool, row_chunk: int = 512,
     return o, lse
 
 
-def attention_fwd_rows(q_head, k_head, v_head, scale: float, causal: bool, rows):
+def attention_fwd_rows(q_head, k_head, v_head, scale: float, causal: bool, rows,
+                       dropout_p: float = 0.0, seed: int = 0, bh: int = 0):
     """O and LSE for selected query rows of one head.
 
     q_head, k_head, v_head: [N, d] fp64 for one (batch, head); rows: positions.
     Each row of attention depends only on its own query and all keys, so a sample of
-    rows is checked against the same definition as the whole tensor.
+    rows is checked against the same definition as the whole tensor.  With dropout the
+    mask is that of head index ``bh``.
     """
     rows = np.asarray(rows, dtype=np.int64)
-    s = scores(np.asarray(q_head, np.float64)[rows], np.asarray(k_head, np.float64),
-               scale, causal, rows)
+    k = np.asarray(k_head, np.float64)
+    s = scores(np.asarray(q_head, np.float64)[rows], k, scale, causal, rows)
     p, m, l = _softmax_rows(s)
+    if dropout_p > 0:
+        p = p * _dropout_z(bh, rows, k.shape[0], dropout_p, seed)
     return p @ np.asarray(v_head, np.float64), m + np.log(l)
 
 
@@ -180,7 +184,8 @@ def attention_bwd(q, k, v, do, scale: float, causal: bool, row_chunk: int = 512,
     return dq, dk, dv, dvec
 
 
-def attention_bwd_rows(q_head, k_head, v_head, do_head, scale: float, causal: bool, rows):
+def attention_bwd_rows(q_head, k_head, v_head, do_head, scale: float, causal: bool, rows,
+                       dropout_p: float = 0.0, seed: int = 0, bh: int = 0):
     """dQ rows and D for selected query rows of one head.
 
     dQ_i = scale * sum_j P_ij (dP_ij - D_i) K_j needs only row i of P, so a sample of
@@ -193,15 +198,17 @@ def attention_bwd_rows(q_head, k_head, v_head, do_head, scale: float, causal: bo
     do = np.asarray(do_head, np.float64)[rows]
     s = scores(q[rows], k, scale, causal, rows)
     p, _, _ = _softmax_rows(s)
-    o = p @ v
+    z = _dropout_z(bh, rows, k.shape[0], dropout_p, seed) if dropout_p > 0 else 1.0
+    o = (p * z) @ v
     dp = do @ v.T
     drow = np.sum(do * o, axis=1)
-    ds = p * (dp - drow[:, None])
+    ds = p * (dp * z - drow[:, None])
     return scale * (ds @ k), drow
 
 
 def attention_bwd_key_columns(q_head, k_head, v_head, do_head, scale: float, causal: bool,
-                              keys, row_chunk: int = 512):
+                              keys, row_chunk: int = 512, dropout_p: float = 0.0, seed: int = 0,
+                              bh: int = 0):
     """dK and dV rows of selected keys of one head, exactly from the definition.
 
     dV_j = sum_i P_ij dO_i and dK_j = scale * sum_i dS_ij Q_i need column j of P and dS over
@@ -222,11 +229,12 @@ def attention_bwd_key_columns(q_head, k_head, v_head, do_head, scale: float, cau
         rows = np.arange(r0, r1)
         s = scores(q[r0:r1], k, scale, causal, rows)
         p, _, _ = _softmax_rows(s)
-        o = p @ v
+        z = _dropout_z(bh, rows, N, dropout_p, seed) if dropout_p > 0 else np.ones_like(p)
+        o = (p * z) @ v
         drow = np.sum(do[r0:r1] * o, axis=1)
-        p_sel = p[:, keys]
-        ds_sel = p_sel * (do[r0:r1] @ v_sel.T - drow[:, None])
-        dv += p_sel.T @ do[r0:r1]
+        p_sel, z_sel = p[:, keys], z[:, keys]
+        ds_sel = p_sel * ((do[r0:r1] @ v_sel.T) * z_sel - drow[:, None])
+        dv += (p_sel * z_sel).T @ do[r0:r1]
         dk += scale * (ds_sel.T @ q[r0:r1])
     return dk, dv
 

@@ -121,3 +121,25 @@ def test_every_sixteen_bit_draw_pattern_is_used():
     assert np.all(np.abs(rates - 0.5) < 5 * sigma)
     # the two halves of one word are not the same draw
     assert np.mean(keep[:, 0::2] == keep[:, 1::2]) < 0.55
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_row_and_column_variants_with_dropout_match_the_whole_head(causal):
+    # the sampled-row / sampled-key variants used at full size are the same definition
+    N, d, p, seed, bh = 37, 8, 0.3, 77, 5
+    q, k, v, do = (rnd((N, d), s) for s in (21, 22, 23, 24))
+    dq, dk, dv, dvec = A.attention_bwd_head(q, k, v, do, 0.4, causal, dropout_p=p, seed=seed, bh=bh)
+    rows = np.array([0, 3, 17, 36])
+    # forward rows against the batched definition (this head placed at index bh)
+    qb, kb, vb = (np.zeros((1, bh + 1, N, d)) for _ in range(3))
+    qb[0, bh], kb[0, bh], vb[0, bh] = q, k, v
+    o_all, lse_all = A.attention_fwd(qb, kb, vb, 0.4, causal, dropout_p=p, seed=seed)
+    o_r, lse_r = A.attention_fwd_rows(q, k, v, 0.4, causal, rows, dropout_p=p, seed=seed, bh=bh)
+    assert np.max(np.abs(o_r - o_all[0, bh, rows])) < 1e-12
+    assert np.max(np.abs(lse_r - lse_all[0, bh, rows])) < 1e-12
+    dq_r, d_r = A.attention_bwd_rows(q, k, v, do, 0.4, causal, rows, dropout_p=p, seed=seed, bh=bh)
+    assert np.max(np.abs(dq_r - dq[rows])) < 1e-12 and np.max(np.abs(d_r - dvec[rows])) < 1e-12
+    keys = np.array([0, 9, 30, 36])
+    dk_c, dv_c = A.attention_bwd_key_columns(q, k, v, do, 0.4, causal, keys, row_chunk=10,
+                                             dropout_p=p, seed=seed, bh=bh)
+    assert np.max(np.abs(dk_c - dk[keys])) < 1e-12 and np.max(np.abs(dv_c - dv[keys])) < 1e-12
