@@ -83,12 +83,14 @@ def test_fp8_forward_scale_and_descales():
     check(to_f64(o), to_f64(lse), o_ref, lse_ref, vmax, "descales")
 
 
-def test_fp8_forward_full_size_sampled_rows():
-    # the long causal language-model shape, 4 x 16 x 8192 x 128: every head checked on sampled
-    # rows (each row of attention depends only on its query and all keys)
-    B, H, N = 4, 16, 8192
-    (q8, k8, v8, (qs, ks, vs)), (tq, tk, tvt) = device_fp8(B, H, N, seed=42)
-    o, lse = fa.forward_fp8(tq, tk, tvt, qs, ks, vs, causal=True)
+@pytest.mark.parametrize("B,causal", [(4, True), (2, False)])
+def test_fp8_forward_full_size_sampled_rows(B, causal):
+    # the long causal language-model shape, 4 x 16 x 8192 x 128, and its non-causal half-batch
+    # sibling: heads checked on sampled rows (each row of attention depends only on its query
+    # and all keys)
+    H, N = 16, 8192
+    (q8, k8, v8, (qs, ks, vs)), (tq, tk, tvt) = device_fp8(B, H, N, seed=42 + B)
+    o, lse = fa.forward_fp8(tq, tk, tvt, qs, ks, vs, causal=causal)
     assert fa.status_check() == abi.FA_OK
     o, lse = to_f64(o), to_f64(lse)
     rng = np.random.default_rng(7)
@@ -99,7 +101,7 @@ def test_fp8_forward_full_size_sampled_rows():
             rows = np.sort(rng.choice(N, 48, replace=False))
             rows[0], rows[-1] = 0, N - 1
             qh, kh, vh = (fp8.e4m3_bits_to_f64(x[b, h]) * s for x, s in ((q8, qs), (k8, ks), (v8, vs)))
-            o_ref, lse_ref = A.attention_fwd_rows(qh, kh, vh, 1 / math.sqrt(128), True, rows)
+            o_ref, lse_ref = A.attention_fwd_rows(qh, kh, vh, 1 / math.sqrt(128), causal, rows)
             bar = 2.0 ** -4 * vmax + 2.0 ** -8 * np.max(np.abs(o_ref))
             assert max_abs(o[b, h, rows], o_ref) <= bar, (b, h)
             assert max_abs(lse[b, h, rows], lse_ref) <= LSE_MAX_ABS, (b, h)
