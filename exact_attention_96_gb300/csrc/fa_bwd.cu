@@ -586,7 +586,7 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
       const uint32_t src = half == 0 ? sQ(0) : sdO(0);
       for (int s = 0; s < L::kSlabs; ++s) tma_store_3d(map, src + s * (kTile * 128), s * 64, k0, bh);
       bulk_commit_group();
-      bulk_wait_group_all();
+      bulk_wait_group_read_all();  // source read: the CTA may exit
     }
   } else if (warp < kProducerWarp) {
     // --------------------------------------------------------- dQ drain ----

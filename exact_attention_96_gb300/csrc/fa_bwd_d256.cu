@@ -339,7 +339,7 @@ fa_bwd_d256_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
       const uint32_t src = half == 0 ? sQ : sdO;
       for (int s = 0; s < 2; ++s) tma_store_3d(map, src + s * (kKeys * 128), kDH * z + 64 * s, k0, bh);
       bulk_commit_group();
-      bulk_wait_group_all();
+      bulk_wait_group_read_all();  // source read: the CTA may exit
     }
   } else if (warp < kProducerWarp) {
     // dQ drain: thread t owns column 128z + t of the head dimension (TMEM lane t of dQ^T)

@@ -412,7 +412,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     if (threadIdx.x == 0 && fin && !split_mode && mbar_wait(bar(L::kBarEpi), 0, wc) && *abort_flag == 0) {
       for (int s = 0; s < L::kSlabs; ++s) tma_store_3d(&tmO, sQ + s * (kBM * 128), s * 64, q0, bh);
       bulk_commit_group();
-      bulk_wait_group_all();
+      bulk_wait_group_read_all();  // source read: the CTA may exit
     }
   }
 

@@ -368,7 +368,7 @@ fa_fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
         const uint32_t src = smem_addr(stage);
         for (int s = 0; s < 2; ++s) tma_store_3d(&tmO, src + s * (kBM * 128), s * 64, q0 + t * kBM, bh);
         bulk_commit_group();
-        bulk_wait_group_all();
+        bulk_wait_group_read_all();  // source read: the CTA may exit
       }
     }
   }
