@@ -242,19 +242,20 @@ def run_gpu(args, rank, world, local_rank):
     if fa.status_check(dev) != abi.FA_OK:
         raise RuntimeError("device status after the timed region is not FA_OK")
 
-    # End-to-end through the public API with host buffers: pinned H2D of q, k, v, dO, the
-    # two calls, D2H of O, LSE, dQ, dK, dV -- every step.
+    # End-to-end through the public API with host buffers (fa.step_host / fa_step_host): every
+    # step copies q, k, v, dO in from pinned host memory, runs the forward and the backward and
+    # copies O, LSE, dQ, dK, dV out, the copies of one chunk of heads overlapping the kernels of
+    # another.
     pin = [torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).pin_memory() for x in host]
-    outs_host = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (o, lse, dq, dk, dv)]
+    outs_host = tuple(torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (o, lse, dq, dk, dv))
     h2d = sum(t.numel() * t.element_size() for t in pin)
     d2h = sum(t.numel() * t.element_size() for t in outs_host)
+    dev_bufs = [q, k, v, do, o, lse, dq, dk, dv]
+    ws_host = torch.empty(abi.fa_step_host_workspace_bytes(B, H, N, d, 0), dtype=torch.uint8, device=dev)
 
     def e2e_step():
-        for src, dst in zip(pin, (q, k, v, do)):
-            dst.copy_(src, non_blocking=True)
-        step()
-        for src, dst in zip((o, lse, dq, dk, dv), outs_host):
-            dst.copy_(src, non_blocking=True)
+        fa.step_host(*pin, causal=causal, scale=scale, out=outs_host, device_buffers=dev_bufs,
+                     workspace=ws_host, device=dev)
 
     e2e_step()
     barrier()

@@ -7,4 +7,4 @@ synthetic inputs, ``build`` compiles the library in-tree.
 """
 
 from .attention import (forward, forward_fp8, forward_splitkv, backward, workspace_bytes,  # noqa: F401
-                        status_check)
+                        step_host, status_check)

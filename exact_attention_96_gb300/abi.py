@@ -55,6 +55,9 @@ SIGNATURES = {
     "fa_bwd_noalloc": (_c_int, [_c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_void_p,
                                 _c_void_p, _c_void_p, _c_void_p,
                                 _c_int, _c_int, _c_int, _c_int, _c_float, _c_int, _c_void_p]),
+    "fa_step_host_workspace_bytes": (_c_size_t, [_c_int] * 5),
+    "fa_step_host": (_c_int, [_c_void_p] * 18 + [_c_int, _c_int, _c_int, _c_int, _c_float, _c_int, _c_int,
+                                                 _c_void_p, _c_size_t, _c_void_p]),
     "fa_status_check": (_c_int, [_c_void_p]),
     "fa_status_string": (ctypes.c_char_p, [_c_int]),
     "fa_set_wait_limit_ns": (ctypes.c_uint64, [ctypes.c_uint64]),
@@ -148,6 +151,16 @@ def fa_bwd_dropout(q, k, v, o, do, lse, dq, dk, dv, B, H, N, d, scale, causal, d
 
 def fa_bwd_noalloc(q, k, v, o, do, lse, dq, dk, dv, B, H, N, d, scale, causal, stream) -> int:
     return load().fa_bwd_noalloc(q, k, v, o, do, lse, dq, dk, dv, B, H, N, d, scale, int(causal), stream)
+
+
+def fa_step_host_workspace_bytes(B, H, N, d, num_chunks) -> int:
+    return load().fa_step_host_workspace_bytes(B, H, N, d, num_chunks)
+
+
+def fa_step_host(host_ptrs, dev_ptrs, B, H, N, d, scale, causal, num_chunks, ws, ws_bytes, stream) -> int:
+    """host_ptrs: (q, k, v, do, o, lse, dq, dk, dv); dev_ptrs: (q, k, v, do, o, lse, dq, dk, dv)."""
+    return load().fa_step_host(*host_ptrs, *dev_ptrs, B, H, N, d, scale, int(causal), num_chunks, ws, ws_bytes,
+                               stream)
 
 
 def fa_status_check(stream) -> int:

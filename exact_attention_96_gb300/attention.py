@@ -123,6 +123,39 @@ def backward(q, k, v, o, do, lse, causal: bool = False, scale: float | None = No
     return dq, dk, dv
 
 
+def step_host(q_h, k_h, v_h, do_h, causal: bool = False, scale: float | None = None, out=None,
+              device_buffers=None, workspace=None, num_chunks: int = 0, device=None):
+    """One forward + backward step with inputs and results in host memory (fa_step_host):
+    the copies of one chunk of heads overlap the kernels of another.  q_h, k_h, v_h, do_h:
+    pinned CPU bf16 [B, H, N, d].  Returns the host results (O, LSE, dQ, dK, dV), written into
+    `out` when given.  device_buffers (q, k, v, dO, O, LSE, dQ, dK, dV on the device) and
+    workspace are allocated when not given; pass them to reuse them across steps.  The call
+    is asynchronous on the current stream, like the others."""
+    for t in (q_h, k_h, v_h, do_h):
+        if t.is_cuda or t.dtype != torch.bfloat16 or not t.is_contiguous() or t.dim() != 4:
+            raise ValueError("expected contiguous bf16 host tensors [B, H, N, d]")
+    B, H, N, d = q_h.shape
+    dev = torch.device("cuda") if device is None else torch.device(device)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    if out is None:
+        out = tuple(torch.empty(q_h.shape, dtype=torch.bfloat16).pin_memory() for _ in range(4))
+        out = (out[0], torch.empty((B, H, N), dtype=torch.float32).pin_memory(), *out[1:])
+    if device_buffers is None:
+        device_buffers = [torch.empty(q_h.shape, dtype=torch.bfloat16, device=dev) for _ in range(5)]
+        device_buffers += [torch.empty((B, H, N), dtype=torch.float32, device=dev)]
+        device_buffers += [torch.empty(q_h.shape, dtype=torch.bfloat16, device=dev) for _ in range(3)]
+    if workspace is None:
+        workspace = torch.empty(abi.fa_step_host_workspace_bytes(B, H, N, d, num_chunks), dtype=torch.uint8,
+                                device=dev)
+    host_ptrs = [t.data_ptr() for t in (q_h, k_h, v_h, do_h, *out)]
+    dev_ptrs = [t.data_ptr() for t in device_buffers]
+    with torch.cuda.device(dev):
+        st = abi.fa_step_host(host_ptrs, dev_ptrs, B, H, N, d, scale, causal, num_chunks,
+                              workspace.data_ptr(), workspace.numel(), torch.cuda.current_stream(dev).cuda_stream)
+    abi.check("fa_step_host", st)
+    return out
+
+
 def status_check(device=None) -> int:
     """Synchronises the current stream and returns the library's device status code."""
     dev = torch.device("cuda") if device is None else torch.device(device)

@@ -194,6 +194,32 @@ fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const void
                          int B, int H, int N, int d, float scale, int causal, fa_stream_t stream);
 
 /*
+ * One attention training step with its inputs and results in host memory (a deployment
+ * convenience; the pages have no counterpart): copies in, fa_fwd, fa_bwd, copies out, with
+ * the copies of one chunk of heads overlapped with the kernels of another (heads are
+ * independent in both passes).
+ *   q_h, k_h, v_h, do_h: host bf16 [B,H,N,d] inputs; o_h, dq_h, dk_h, dv_h: host bf16
+ *   [B,H,N,d] and lse_h: host fp32 [B,H,N] results.  Pinned (page-locked) host memory is
+ *   needed for the copies to overlap; pageable memory works but serialises them.
+ *   q, k, v, dout, o, dq, dk, dv (bf16 [B,H,N,d]) and lse (fp32 [B,H,N]): caller-owned
+ *   device buffers the step runs in; on return they hold the step's device copies.
+ *   num_chunks: chunks of heads (<= 64; <= 0: 8); workspace: device, 256-byte aligned,
+ *   >= fa_step_host_workspace_bytes(B,H,N,d,num_chunks) bytes (0: invalid sizes).
+ * Streams: the copies run on two library-owned streams of the current device and the kernels
+ * of alternate chunks on `stream` and on a third library-owned stream, all ordered after the
+ * caller's earlier work on `stream`; `stream` completes after the last copy out.  Calls are enqueued one at a time (an internal lock).  No dropout
+ * (its mask depends on the absolute head index).  Errors as for fa_fwd / fa_bwd; an error
+ * during enqueueing may leave part of the step enqueued.
+ */
+size_t fa_step_host_workspace_bytes(int B, int H, int N, int d, int num_chunks);
+fa_status fa_step_host(const void* q_h, const void* k_h, const void* v_h, const void* do_h,
+                       void* o_h, float* lse_h, void* dq_h, void* dk_h, void* dv_h,
+                       void* q, void* k, void* v, void* dout, void* o, float* lse,
+                       void* dq, void* dk, void* dv, int B, int H, int N, int d, float scale,
+                       int causal, int num_chunks, void* workspace, size_t workspace_bytes,
+                       fa_stream_t stream);
+
+/*
  * Synchronises `stream`, then reads and clears the current device's error word.
  * Returns FA_OK, FA_ERR_TIMEOUT (a kernel's bounded wait gave up; its outputs are
  * undefined) or FA_ERR_CUDA (the synchronisation itself failed).

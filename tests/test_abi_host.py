@@ -169,3 +169,24 @@ def test_fp8_forward_argument_checks_before_launch(lib):
     assert call(q8=0) == abi.FA_ERR_INVALID_ARG
     assert call(vt8=FAKE + 8) == abi.FA_ERR_MISALIGNED
     assert call(N=0) == abi.FA_ERR_INVALID_ARG
+
+
+def test_step_host_argument_checks_before_launch(lib):
+    def call(**kw):
+        a = dict(ptrs=[FAKE] * 18, B=1, H=2, N=128, d=64, scale=0.125, causal=0, chunks=0, ws=FAKE,
+                 ws_bytes=1 << 30, stream=None)
+        a.update(kw)
+        return abi.fa_step_host(a["ptrs"][:9], a["ptrs"][9:], a["B"], a["H"], a["N"], a["d"], a["scale"],
+                                a["causal"], a["chunks"], a["ws"], a["ws_bytes"], a["stream"])
+    assert call(ptrs=[FAKE] * 17 + [0]) == abi.FA_ERR_INVALID_ARG
+    assert call(ws=0) == abi.FA_ERR_INVALID_ARG
+    assert call(N=0) == abi.FA_ERR_INVALID_ARG
+    assert call(chunks=65) == abi.FA_ERR_UNSUPPORTED
+    assert call(d=96) == abi.FA_ERR_UNSUPPORTED
+    assert call(ws_bytes=16) == abi.FA_ERR_INVALID_ARG
+    # the workspace covers the largest chunk's backward
+    def two(n):  # one 256-byte aligned workspace per compute stream
+        return 2 * ((n + 255) // 256 * 256)
+    assert abi.fa_step_host_workspace_bytes(1, 8, 128, 64, 4) == two(abi.fa_bwd_workspace_bytes(1, 2, 128, 64))
+    assert abi.fa_step_host_workspace_bytes(1, 8, 130, 64, 4) == two(abi.fa_bwd_workspace_bytes(1, 4, 130, 64))
+    assert abi.fa_step_host_workspace_bytes(1, 8, 128, 64, 65) == 0
