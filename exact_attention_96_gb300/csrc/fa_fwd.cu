@@ -295,27 +295,29 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         for (int c = 0; c < BC; ++c)
           if (c >= lim) s[c] = -INFINITY;
       }
-      float mx0 = s[0], mx1 = s[1];
+      // row maximum: two chains of three-input maxima
+      float mx0 = fmaxf(s[0], s[1]), mx1 = fmaxf(s[2], s[3]);
 #pragma unroll
-      for (int c = 2; c < BC; c += 2) {
-        mx0 = fmaxf(mx0, s[c]);
-        mx1 = fmaxf(mx1, s[c + 1]);
+      for (int c = 4; c < BC; c += 4) {
+        mx0 = fmax3(mx0, s[c], s[c + 1]);
+        mx1 = fmax3(mx1, s[c + 2], s[c + 3]);
       }
       const float m_new = fmaxf(m_run, fmaxf(mx0, mx1) * sl2);
       const float alpha = ex2_approx(m_run - m_new);  // 0 on the first tile
       const bool grew = (j > 0) && (m_new > m_run);
       m_run = m_new;
       const float neg_m = -m_new;
-      float sum0 = 0.f, sum1 = 0.f;
+      float2 sum2 = make_float2(0.f, 0.f);  // (even keys, odd keys)
       uint32_t pk[BC / 2];
       [[maybe_unused]] uint4 dw;  // dropout: words of keys c .. c+7
       [[maybe_unused]] const uint32_t t_lo = args.dropout.threshold, t_hi = args.dropout.threshold << 16;
 #pragma unroll
       for (int c = 0; c < BC; c += 2) {
-        const float p0 = ex2_approx(fmaf(s[c], sl2, neg_m));
-        const float p1 = ex2_approx(fmaf(s[c + 1], sl2, neg_m));
-        sum0 += p0;
-        sum1 += p1;
+        // two keys per instruction for the scaling and the sums (same rounding as scalar)
+        const float2 x = ffma2(make_float2(s[c], s[c + 1]), make_float2(sl2, sl2), make_float2(neg_m, neg_m));
+        const float p0 = ex2_approx(x.x);
+        const float p1 = ex2_approx(x.y);
+        sum2 = fadd2(sum2, make_float2(p0, p1));
         if constexpr (DROPOUT) {
           // key c (even) is the low half of its word, key c + 1 the high half; the undropped
           // values stay in the sums
@@ -326,7 +328,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
           pk[c / 2] = pack_bf16x2(p0, p1);
         }
       }
-      l_run = l_run * alpha + (sum0 + sum1);
+      l_run = l_run * alpha + (sum2.x + sum2.y);
       // P_j into its TMEM buffer (its previous reader, P_{j-2} V_{j-2}, finished before
       // S_j was signalled).
 #pragma unroll
@@ -347,7 +349,12 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             uint32_t r[32];
             tmem_ld32(tmem + lane_off + L::kColO + c, r);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+            for (int i = 0; i < 32; i += 2) {
+              const float2 y = fmul2(make_float2(__uint_as_float(r[i]), __uint_as_float(r[i + 1])),
+                                     make_float2(alpha, alpha));
+              r[i] = __float_as_uint(y.x);
+              r[i + 1] = __float_as_uint(y.y);
+            }
             tmem_st32(tmem + lane_off + L::kColO + c, r);
           }
         } else {
