@@ -7,8 +7,9 @@
 //   dQ = scale * dS K,  dK = scale * dS^T Q.
 //
 // Three launches on one stream:
-//   1. fa_bwd_prep_kernel   D = rowsum(dO * O), LSE2 = LSE * log2(e) (both fp32, rows padded
-//                           to a multiple of 4), and a zeroed fp32 dQ accumulator.
+//   1. fa_bwd_prep_kernel   D = rowsum(dO * O), LSE2 = LSE * log2(e) (both fp32, stored
+//                           negated, rows padded to a multiple of 4), and a zeroed fp32 dQ
+//                           accumulator.
 //   2. fa_bwd_main_kernel   one CTA per tile of 128 keys of one (batch, head); it keeps K_j,
 //                           V_j and the dK_j, dV_j accumulators on chip and loops over the
 //                           query tiles, adding each tile's dQ contribution into the fp32
@@ -99,8 +100,9 @@ fa_bwd_prep_kernel(const uint16_t* __restrict__ o, const uint16_t* __restrict__ 
 #pragma unroll
   for (int w = kTPR / 2; w >= 1; w >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, w);
   if (sub == 0 && i < Np) {
-    dvec[(size_t)bh * Np + i] = (i < N) ? acc : 0.f;
-    lse2[(size_t)bh * Np + i] = (i < N) ? lse[(size_t)bh * N + i] * kLog2e : 0.f;
+    // stored negated: the main kernels add them with two-wide instructions
+    dvec[(size_t)bh * Np + i] = (i < N) ? -acc : 0.f;
+    lse2[(size_t)bh * Np + i] = (i < N) ? -(lse[(size_t)bh * N + i] * kLog2e) : 0.f;
   }
 }
 
@@ -472,8 +474,11 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
         uint32_t w[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
-          float p0 = ex2_approx(fmaf(__uint_as_float(r[e]), sl2, -lv[e]));
-          float p1 = ex2_approx(fmaf(__uint_as_float(r[e + 1]), sl2, -lv[e + 1]));
+          // lv holds -LSE * log2(e): two keys' exponents in one instruction
+          const float2 x = ffma2(make_float2(__uint_as_float(r[e]), __uint_as_float(r[e + 1])),
+                                 make_float2(sl2, sl2), make_float2(lv[e], lv[e + 1]));
+          float p0 = ex2_approx(x.x);
+          float p1 = ex2_approx(x.y);
           if (edge) {
             const int qa = q0 + c0 + cc + e;
             if (qa >= N || (CAUSAL && qa < key)) p0 = 0.f;
@@ -531,8 +536,9 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
             dp0 = (kb & 1u) ? dp0 * args.dropout.scale : 0.f;
             dp1 = (kb & 2u) ? dp1 * args.dropout.scale : 0.f;
           }
-          float ds0 = p0 * (dp0 - dl[e]);
-          float ds1 = p1 * (dp1 - dl[e + 1]);
+          // dl holds -D: dS = P (dP - D) two at a time
+          const float2 ds = fmul2(make_float2(p0, p1), fadd2(make_float2(dp0, dp1), make_float2(dl[e], dl[e + 1])));
+          float ds0 = ds.x, ds1 = ds.y;
           if (edge) {
             const int qa = q0 + c0 + cc + e;
             if (qa >= N) ds0 = 0.f;

@@ -256,8 +256,9 @@ fa_bwd_d256_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
         uint32_t w[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
-          float p0 = ex2_approx(fmaf(__uint_as_float(r[e]), sl2, -lse2[e]));
-          float p1 = ex2_approx(fmaf(__uint_as_float(r[e + 1]), sl2, -lse2[e + 1]));
+          // lse2 holds -LSE * log2(e) (stored negated by the prep kernel)
+          float p0 = ex2_approx(fmaf(__uint_as_float(r[e]), sl2, lse2[e]));
+          float p1 = ex2_approx(fmaf(__uint_as_float(r[e + 1]), sl2, lse2[e + 1]));
           if (edge) {
             const int qa = q0 + c0 + e;
             if (qa >= N || (CAUSAL && qa < key)) p0 = 0.f;
@@ -285,8 +286,9 @@ fa_bwd_d256_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
         for (int e = 0; e < 32; e += 2) {
           const float p0 = __uint_as_float(pr[e / 2] << 16);
           const float p1 = __uint_as_float(pr[e / 2] & 0xFFFF0000u);
-          float ds0 = p0 * (__uint_as_float(r[e]) - dvv[e]);
-          float ds1 = p1 * (__uint_as_float(r[e + 1]) - dvv[e + 1]);
+          // dvv holds -D
+          float ds0 = p0 * (__uint_as_float(r[e]) + dvv[e]);
+          float ds1 = p1 * (__uint_as_float(r[e + 1]) + dvv[e + 1]);
           if (edge) {
             const int qa = q0 + c0 + e;
             if (qa >= N) ds0 = 0.f;

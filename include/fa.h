@@ -118,8 +118,9 @@ fa_status fa_merge_partials(const float* o_parts, const float* lse_parts, int nu
                             long long rows, int d, void* o, float* lse, fa_stream_t stream);
 
 /*
- * Bytes of device workspace fa_bwd needs: D [B,H,N] fp32 followed (at a 256-byte aligned
- * offset) by the fp32 dQ accumulator [B,H,N,d].  Returns 0 for invalid sizes.
+ * Bytes of device workspace fa_bwd needs: -D and -LSE * log2(e) ([B,H,N] fp32 each, rows
+ * padded to a multiple of 4), then, at 256-byte aligned offsets, the fp32 dQ accumulator
+ * [B,H,N,d].  Returns 0 for invalid sizes.
  */
 size_t fa_bwd_workspace_bytes(int B, int H, int N, int d);
 
@@ -128,7 +129,8 @@ size_t fa_bwd_workspace_bytes(int B, int H, int N, int d);
  * by fa_fwd for the same q, k, v, scale and causal flag.  Outputs dq, dk, dv: bf16
  * [B,H,N,d] (written).  workspace: caller-owned device buffer of at least
  * fa_bwd_workspace_bytes(B,H,N,d) bytes, 256-byte aligned; its contents on entry do not
- * matter and on return hold D = rowsum(dO * O) and the fp32 dQ accumulator.
+ * matter and on return hold -D (D = rowsum(dO * O)), -LSE * log2(e) and the fp32 dQ
+ * accumulator.
  * Steps (one stream, no host synchronisation): D and a zeroed dQ accumulator; one pass
  * over key/value tiles that recomputes S and P and produces dK, dV and accumulates dQ;
  * dQ conversion to bf16.
