@@ -289,33 +289,33 @@ fa_fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
         for (int c = 0; c < kBC; ++c)
           if (c >= lim) s[c] = -INFINITY;
       }
-      float mx0 = s[0], mx1 = s[1];
+      float mx0 = fmaxf(s[0], s[1]), mx1 = fmaxf(s[2], s[3]);
 #pragma unroll
-      for (int c = 2; c < kBC; c += 2) {
-        mx0 = fmaxf(mx0, s[c]);
-        mx1 = fmaxf(mx1, s[c + 1]);
+      for (int c = 4; c < kBC; c += 4) {
+        mx0 = fmax3(mx0, s[c], s[c + 1]);
+        mx1 = fmax3(mx1, s[c + 2], s[c + 3]);
       }
       const float m_new = fmaxf(m_run, fmaxf(mx0, mx1) * sl2);
       const float alpha = ex2_approx(m_run - m_new);  // 0 on the first tile
       const bool grew = (j > 0) && (m_new > m_run);
       m_run = m_new;
       const float neg_m = kPBias - m_new;
-      float sum0 = 0.f, sum1 = 0.f;
+      float2 sum2 = make_float2(0.f, 0.f);
       // P_j into the first columns of S_j (all of S_j is in registers; the tensor core
       // touches this tile's S again only after P_j V_j)
       uint32_t pk[kBC / 4];
 #pragma unroll
       for (int c = 0; c < kBC; c += 4) {
-        const float p0 = ex2_approx(fmaf(s[c], sl2, neg_m));
-        const float p1 = ex2_approx(fmaf(s[c + 1], sl2, neg_m));
-        const float p2 = ex2_approx(fmaf(s[c + 2], sl2, neg_m));
-        const float p3 = ex2_approx(fmaf(s[c + 3], sl2, neg_m));
-        sum0 += p0 + p2;
-        sum1 += p1 + p3;
+        // two keys per instruction for the scaling and the sums
+        const float2 x01 = ffma2(make_float2(s[c], s[c + 1]), make_float2(sl2, sl2), make_float2(neg_m, neg_m));
+        const float2 x23 = ffma2(make_float2(s[c + 2], s[c + 3]), make_float2(sl2, sl2), make_float2(neg_m, neg_m));
+        const float p0 = ex2_approx(x01.x), p1 = ex2_approx(x01.y);
+        const float p2 = ex2_approx(x23.x), p3 = ex2_approx(x23.y);
+        sum2 = fadd2(sum2, fadd2(make_float2(p0, p1), make_float2(p2, p3)));
         pk[c / 4] = pack_e4m3x4(p0, p1, p2, p3);
       }
       tmem_st32(tcol, pk);
-      l_run = l_run * alpha + (sum0 + sum1);
+      l_run = l_run * alpha + (sum2.x + sum2.y);
       // Rescale the accumulator when this warp's rows saw a larger maximum.  O holds
       // P_0 V_0 .. P_{j-1} V_{j-1}, all complete: S_j was issued after the last of them had
       // landed, and its commit covers them.
@@ -325,7 +325,12 @@ fa_fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
           uint32_t r[32];
           tmem_ld32(tcol + L::kColO + c, r);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+          for (int i = 0; i < 32; i += 2) {
+            const float2 y = fmul2(make_float2(__uint_as_float(r[i]), __uint_as_float(r[i + 1])),
+                                   make_float2(alpha, alpha));
+            r[i] = __float_as_uint(y.x);
+            r[i + 1] = __float_as_uint(y.y);
+          }
           tmem_st32(tcol + L::kColO + c, r);
         }
       }
