@@ -256,9 +256,11 @@ fa_bwd_d256_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
         uint32_t w[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
-          // lse2 holds -LSE * log2(e) (stored negated by the prep kernel)
-          float p0 = ex2_approx(fmaf(__uint_as_float(r[e]), sl2, lse2[e]));
-          float p1 = ex2_approx(fmaf(__uint_as_float(r[e + 1]), sl2, lse2[e + 1]));
+          // lse2 holds -LSE * log2(e) (stored negated by the prep kernel): two keys per instruction
+          const float2 x = ffma2(make_float2(__uint_as_float(r[e]), __uint_as_float(r[e + 1])),
+                                 make_float2(sl2, sl2), make_float2(lse2[e], lse2[e + 1]));
+          float p0 = ex2_approx(x.x);
+          float p1 = ex2_approx(x.y);
           if (edge) {
             const int qa = q0 + c0 + e;
             if (qa >= N || (CAUSAL && qa < key)) p0 = 0.f;
@@ -286,9 +288,10 @@ fa_bwd_d256_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
         for (int e = 0; e < 32; e += 2) {
           const float p0 = __uint_as_float(pr[e / 2] << 16);
           const float p1 = __uint_as_float(pr[e / 2] & 0xFFFF0000u);
-          // dvv holds -D
-          float ds0 = p0 * (__uint_as_float(r[e]) + dvv[e]);
-          float ds1 = p1 * (__uint_as_float(r[e + 1]) + dvv[e + 1]);
+          // dvv holds -D: dS = P (dP - D) two at a time
+          const float2 ds = fmul2(make_float2(p0, p1), fadd2(make_float2(__uint_as_float(r[e]), __uint_as_float(r[e + 1])),
+                                                             make_float2(dvv[e], dvv[e + 1])));
+          float ds0 = ds.x, ds1 = ds.y;
           if (edge) {
             const int qa = q0 + c0 + e;
             if (qa >= N) ds0 = 0.f;
