@@ -16,22 +16,24 @@
 //                           accumulator in global memory (no second pass over S).
 //   3. fa_bwd_dq_kernel     dQ accumulator * scale -> bf16 dQ.
 //
-// fa_bwd_main_kernel roles (thread t of a warpgroup owns TMEM lane t):
-//   warps 0-3  key rows: P^T = 2^(S^T*scale*log2e - LSE2) (masked) -> bf16 into TMEM for
-//              the dV product; dS^T = P^T (dP^T - D) -> bf16 into shared memory for the dK
-//              and dQ products; finally dK, dV -> bf16 -> TMA stores.
-//   warps 4-7  query rows: read each finished dQ tile from TMEM and add it (fp32 vector
-//              atomics, coalesced by the accumulator's tile layout) into global memory.
-//   warp 8     TMA producer: K_j, V_j once; then Q_i, dO_i, LSE2_i, D_i through a ring.
-//   warp 9     TMEM allocator and MMA issuer:
-//                S^T  = K_j Q_i^T        (SS)  -> TMEM [0,128)
-//                dP^T = V_j dO_i^T       (SS)  -> TMEM [128,256)
-//                dV  += P^T dO_i         (TS, P^T from TMEM [0,64))
-//                dK  += dS^T Q_i         (SS, dS^T K-major in smem)
-//                dQ_i = dS K_j           (SS, the same dS^T buffer read M-major) -> TMEM [128,..)
-//   The dQ tile reuses the dP^T columns (dP^T is fully read before dS is published), and the
-//   next S^T overwrites P^T only after the dV product that reads it has completed.
-//
+// fa_bwd_main_kernel roles (448 threads; thread t of a warpgroup owns TMEM lane t):
+//   warps 0-7   key rows, two warpgroups splitting each query tile's 128 columns in halves
+//               of 64: P^T = 2^(S^T*scale*log2e - LSE2) (masked) -> bf16 into TMEM for the
+//               dV product (kept in registers too); dS^T = P^T (dP^T - D) -> bf16 into
+//               shared memory for the dK and dQ products; finally dV (first warpgroup) and
+//               dK (second) -> bf16 -> TMA stores.
+//   warps 8-11  dQ drain: read each finished dQ tile from TMEM and add it (fp32 vector
+//               atomics, coalesced by the accumulator's tile layout) into global memory.
+//   warp 12     TMA producer: K_j, V_j once; then Q_i, dO_i, LSE2_i, D_i through a ring.
+//   warp 13     TMEM allocator and MMA issuer; per query tile i, in this order:
+//                 dV  += P^T dO_i         (TS, P^T from TMEM inside the S^T columns)
+//                 S^T_{i+1} = K_j Q^T     (SS, once dV_i has completed) -> TMEM [0,128)
+//                 dQ_i = dS K_j           (SS, dS^T read M-major) -> TMEM [128,..), signalled
+//                 dK  += dS^T Q_i         (SS, dS^T K-major)
+//                 dP^T_{i+1} = V_j dO^T   (SS, once the drain has read dQ_i) -> TMEM [128,256)
+//   so the tensor core runs dV_i and S_{i+1} while the key rows compute dS_i, and dQ_i, dK_i
+//   while they compute P_{i+1}.
+
 // dQ accumulator layout (fp32): [B*H][q tile][d/4][128 rows][4] -- for a fixed group of four
 // columns, the 128 rows of a tile are contiguous, so the 32 lanes of a warp adding one
 // float4 each touch one contiguous 512-byte span.

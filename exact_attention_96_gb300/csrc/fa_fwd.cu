@@ -11,7 +11,10 @@
 //   warps 0-3  softmax: thread t owns query row t (= TMEM lane t).  Reads S from TMEM,
 //              masks, updates (m, l), writes P (bf16) back to TMEM, rescales O in TMEM
 //              when its warp's maximum grew, and finally normalises O, stages it in
-//              shared memory for a TMA store and writes LSE.
+//              shared memory for a TMA store and writes LSE.  The scaling, sums and
+//              rescale run two elements per instruction (fma/add/mul .f32x2) and the row
+//              maximum three at a time: this warp's instruction count is on the critical
+//              path.
 //   warp 4     TMA producer: Q once, then K_j and V_j through an NS-stage ring.
 //   warp 5     TMEM allocator and MMA issuer (one thread):
 //                S_j = Q K_j^T        (tcgen05.mma, A and B from shared memory)
@@ -22,18 +25,19 @@
 // P0 / P1 bf16 pairs [2BC, 2BC + BC/2) and [2BC + BC/2, 3BC), O [3BC, 3BC + D).
 //
 // Shared memory, 1024-byte aligned (128-byte swizzle atoms): Q [D/64 slabs x 128 rows x
-// 128 B], K ring, V ring (each [D/64 slabs x BC rows x 128 B] per stage), barriers.
+// 128 B], K ring, V ring (each [D/64 slabs x BC rows x 128 B] per stage), the dropout
+// generator words (dropout only), barriers.
 // The Q region is reused to stage the bf16 output tile for the TMA store.
 //
 // Every wait is bounded (see WaitCtl): on timeout the kernel records the error, skips the
 // rest of the work, waits for its own copies and MMAs to land and frees TMEM.
 //
 // Dropout (template flag; "FlashAttention 与显存" §07: applied inside the fused kernel): a
-// softmax thread draws the keep bits of its row for the coming key tile (one generator call
-// per 8 keys, philox.cuh) before it waits for S, so the integer work overlaps the Q K^T
-// product.  P enters the P V product with dropped entries zeroed; the running sum l and the
-// LSE are those of the undropped P, and the inverse keep probability is folded into the final
-// 1 / l.
+// softmax thread runs the generator for its row over the coming key tile (one call per 8
+// keys, philox.cuh) before it waits for S, and stages the words in its own shared-memory
+// slots; the softmax reads them back per 8 keys.  P enters the P V product with dropped
+// entries zeroed; the running sum l and the LSE are those of the undropped P, and the
+// inverse keep probability is folded into the final 1 / l.
 
 #include <cuda.h>
 #include <cuda_runtime.h>
