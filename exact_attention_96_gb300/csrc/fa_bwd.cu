@@ -250,8 +250,10 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int bh = blockIdx.y;
-  const int kv_tile = blockIdx.x;
+  // causal: key tile 0 (seen by every query tile) is the heaviest; heads in small groups
+  const RankHead rh = CAUSAL ? causal_dispatch_order() : RankHead{int(blockIdx.x), int(blockIdx.y)};
+  const int bh = rh.bh;
+  const int kv_tile = rh.rank;
   const int k0 = kv_tile * kTile;
   const int N = args.N;
   const int n_q_tiles = (N + kTile - 1) / kTile;

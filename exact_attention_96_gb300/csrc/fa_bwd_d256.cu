@@ -74,9 +74,10 @@ fa_bwd_d256_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
   uint8_t* smem = smem_raw;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int bh = blockIdx.y;
+  const RankHead rh = CAUSAL ? causal_dispatch_order() : RankHead{int(blockIdx.x), int(blockIdx.y)};
+  const int bh = rh.bh;
   const int z = blockIdx.z;               // d slice [128z, 128z + 128)
-  const int k0 = blockIdx.x * kKeys;
+  const int k0 = rh.rank * kKeys;         // causal: key tile 0 is the heaviest
   const int N = args.N;
   const int n_qt = (N + kQ - 1) / kQ;     // 64-row query tiles
   const int it_first = CAUSAL ? (k0 / kQ) : 0;

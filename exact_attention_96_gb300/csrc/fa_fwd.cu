@@ -105,8 +105,10 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int bh = blockIdx.y;
-  const int q_tile = CAUSAL ? (args.n_q_tiles - 1 - int(blockIdx.x)) : int(blockIdx.x);
+  // causal: heavy query tiles (late rows see more keys) first, heads in small groups
+  const RankHead rh = CAUSAL ? causal_dispatch_order() : RankHead{int(blockIdx.x), int(blockIdx.y)};
+  const int bh = rh.bh;
+  const int q_tile = CAUSAL ? (args.n_q_tiles - 1 - rh.rank) : rh.rank;
   const int q0 = q_tile * kBM;
   const int N = args.N;    // query rows
   const int Nk = args.Nk;  // keys

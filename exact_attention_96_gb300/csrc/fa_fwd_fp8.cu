@@ -95,9 +95,10 @@ fa_fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int bh = blockIdx.y;
+  const RankHead rh = CAUSAL ? causal_dispatch_order() : RankHead{int(blockIdx.x), int(blockIdx.y)};
+  const int bh = rh.bh;
   const int n_pairs = (args.n_q_tiles + 1) / 2;
-  const int pair = CAUSAL ? (n_pairs - 1 - int(blockIdx.x)) : int(blockIdx.x);  // heavy pairs first
+  const int pair = CAUSAL ? (n_pairs - 1 - rh.rank) : rh.rank;  // heavy pairs first
   const int q0 = pair * 2 * kBM;  // first row of tile 0; tile 1 starts at q0 + kBM
   const int N = args.N;
   const int n_kv_all = (N + kBC - 1) / kBC;

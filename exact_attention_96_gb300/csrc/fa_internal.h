@@ -11,6 +11,29 @@
 
 namespace fa {
 
+#ifdef __CUDACC__
+// Dispatch order of causal launches.  A causal CTA's work depends on its tile: with rank
+// 0 the heaviest tile of a head, the CTA of rank r processes about (tiles - r) tiles.
+// Dispatched head after head, the last head's heaviest CTA starts near the end and runs
+// alone.  Instead the heads are taken in groups of kCausalGroup, and inside a group every
+// head's rank-r CTA is dispatched before any rank-(r + 1) CTA: the heavy CTAs start first,
+// and the few heads in flight still share their streamed tiles (and the dQ accumulator) in
+// L2.  Maps the CTA's linear index in the (gridDim.x = tiles, gridDim.y = heads) grid to its
+// (rank, head); a bijection for any sizes.
+constexpr int kCausalGroup = 8;
+struct RankHead {
+  int rank, bh;
+};
+__device__ __forceinline__ RankHead causal_dispatch_order() {
+  const int tiles = int(gridDim.x), heads = int(gridDim.y);
+  const int l = int(blockIdx.x) + tiles * int(blockIdx.y);
+  const int g0 = l / (kCausalGroup * tiles) * kCausalGroup;
+  const int gs = min(kCausalGroup, heads - g0);
+  const int r = l - g0 * tiles;
+  return {r / gs, g0 + r % gs};
+}
+#endif
+
 // Everything a forward launch needs besides the four tensor maps.
 struct FwdArgs {
   float* lse;           // [B*H, N] fp32

@@ -131,6 +131,7 @@ BWD = [
     (1, 1, 640, 128, True, 0.2),
     (1, 2, 383, 64, False, 0.3),
     (2, 4, 1024, 128, True, 0.1),
+    (3, 3, 260, 64, True, 0.2),  # causal heads in a full group of eight and a partial one
 ]
 
 

@@ -60,6 +60,7 @@ FP8_SMALL = [
     (1, 2, 640, True),    # five tiles: two full pairs and a half pair
     (1, 1, 1000, False),  # V^T row stride padded to 1008
     (2, 2, 768, False),
+    (11, 1, 520, True),   # causal heads in a full group of eight and a partial one
 ]
 
 

@@ -134,6 +134,23 @@ def test_backward_small(B, H, N, d, causal):
     check_grad(to_f64(dv), dv_ref, "dv")
 
 
+# Causal launches take the heads in groups of eight and, inside a group, every head's
+# heaviest tile first: head counts that fill one group and leave a partial second one,
+# every head compared with the oracle.
+@pytest.mark.parametrize("B,H,N,d", [(3, 5, 300, 64), (11, 1, 260, 128), (2, 5, 200, 256)])
+def test_causal_many_heads(B, H, N, d):
+    (q, k, v, do), (o, lse, dq, dk, dv) = fwd_bwd(B, H, N, d, True, seed=B * H + N)
+    scale = 1 / math.sqrt(d)
+    o_ref, lse_ref = A.attention_fwd(widen(q), widen(k), widen(v), scale, True)
+    check_fwd(to_f64(o), to_f64(lse), o_ref, lse_ref, (B, H, N, d))
+    dq_ref, dk_ref, dv_ref, _ = A.attention_bwd(widen(q), widen(k), widen(v), widen(do), scale, True)
+    for name, g, r in (("dq", dq, dq_ref), ("dk", dk, dk_ref), ("dv", dv, dv_ref)):
+        g = to_f64(g)
+        for b in range(B):
+            for h in range(H):
+                check_grad(g[b, h], r[b, h], (name, b, h))
+
+
 def test_backward_workspace_reuse_is_deterministic_up_to_atomics():
     # dQ is reduced with fp32 atomics (order varies); dK, dV are bitwise reproducible.
     host, (tq, tk, tv, tdo) = device_inputs(1, 2, 384, 128, seed=3)
