@@ -57,11 +57,19 @@ fa_status pipe_for_device(HostPipe** out) {
   return FA_OK;
 }
 
-// Heads per chunk: BH / requested chunks (8 by default), rounded up so that every chunk
-// starts LSE on a 16-byte boundary (heads * N a multiple of 4).
+// Heads per chunk: BH / requested chunks; by default BH / 16, but no fewer heads than give a
+// launch 1.5 waves of 128-row tiles on a 152-SM part (smaller launches leave SMs idle: one
+// head per chunk of the 4x16x8192x128 step ran at half the speed of four).  Rounded up so
+// that every chunk starts LSE on a 16-byte boundary (heads * N a multiple of 4).
 int heads_per_chunk(int BH, int N, int requested) {
-  const int n = std::max(1, std::min({requested > 0 ? requested : 8, BH, kMaxChunks}));
-  int per = (BH + n - 1) / n;
+  int per;
+  if (requested > 0) {
+    const int n = std::max(1, std::min({requested, BH, kMaxChunks}));
+    per = (BH + n - 1) / n;
+  } else {
+    const int tiles = (N + 127) / 128;
+    per = std::max((BH + 15) / 16, (228 + tiles - 1) / tiles);
+  }
   if (N % 4 != 0) per = (per + 3) / 4 * 4;
   return std::min(per, BH);
 }

@@ -205,7 +205,8 @@ fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const void
  *   needed for the copies to overlap; pageable memory works but serialises them.
  *   q, k, v, dout, o, dq, dk, dv (bf16 [B,H,N,d]) and lse (fp32 [B,H,N]): caller-owned
  *   device buffers the step runs in; on return they hold the step's device copies.
- *   num_chunks: chunks of heads (<= 64; <= 0: 8); workspace: device, 256-byte aligned,
+ *   num_chunks: chunks of heads (<= 64; <= 0: 16, fewer when N is short: each chunk keeps
+ *   at least 1.5 waves of 128-row tiles on a 152-SM part); workspace: device, 256-byte aligned,
  *   >= fa_step_host_workspace_bytes(B,H,N,d,num_chunks) bytes (0: invalid sizes).
  * Streams: the copies run on two library-owned streams of the current device and the kernels
  * of alternate chunks on `stream` and on a third library-owned stream, all ordered after the

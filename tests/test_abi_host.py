@@ -190,3 +190,7 @@ def test_step_host_argument_checks_before_launch(lib):
     assert abi.fa_step_host_workspace_bytes(1, 8, 128, 64, 4) == two(abi.fa_bwd_workspace_bytes(1, 2, 128, 64))
     assert abi.fa_step_host_workspace_bytes(1, 8, 130, 64, 4) == two(abi.fa_bwd_workspace_bytes(1, 4, 130, 64))
     assert abi.fa_step_host_workspace_bytes(1, 8, 128, 64, 65) == 0
+    # default: BH / 16 heads per chunk, but at least 1.5 waves of 128-row tiles (228 tiles)
+    assert abi.fa_step_host_workspace_bytes(4, 16, 8192, 128, 0) == two(abi.fa_bwd_workspace_bytes(1, 4, 8192, 128))
+    assert abi.fa_step_host_workspace_bytes(2, 16, 2048, 64, 0) == two(abi.fa_bwd_workspace_bytes(1, 15, 2048, 64))
+    assert abi.fa_step_host_workspace_bytes(1, 8, 128, 64, 0) == two(abi.fa_bwd_workspace_bytes(1, 8, 128, 64))
