@@ -30,7 +30,9 @@
 //                 S^T_{i+1} = K_j Q^T     (SS, once dV_i has completed) -> TMEM [0,128)
 //                 dQ_i = dS K_j           (SS, dS^T read M-major) -> TMEM [128,..), signalled
 //                 dK  += dS^T Q_i         (SS, dS^T K-major)
-//                 dP^T_{i+1} = V_j dO^T   (SS, once the drain has read dQ_i) -> TMEM [128,256)
+//                 dP^T_{i+1} = V_j dO^T   (SS, once the drain has read the dQ_i columns under
+//                                          it; at d = 128 in two halves of 64 queries, one per
+//                                          key-row warpgroup) -> TMEM [128,256)
 //   so the tensor core runs dV_i and S_{i+1} while the key rows compute dS_i, and dQ_i, dK_i
 //   while they compute P_{i+1}.
 
@@ -180,13 +182,13 @@ struct BwdLayout {
   static constexpr int kBarQFull = 1;
   static constexpr int kBarQEmpty = kBarQFull + NS;
   static constexpr int kBarSFull = kBarQEmpty + NS;
-  static constexpr int kBarDPFull = kBarSFull + 1;
-  static constexpr int kBarPReady = kBarDPFull + 1;
+  static constexpr int kBarDPFull = kBarSFull + 1;    // 2: one per query half
+  static constexpr int kBarPReady = kBarDPFull + 2;
   static constexpr int kBarDSReady = kBarPReady + 1;
   static constexpr int kBarDVDone = kBarDSReady + 1;
   static constexpr int kBarDQFull = kBarDVDone + 1;
-  static constexpr int kBarDQDrained = kBarDQFull + 1;
-  static constexpr int kBarDSFree = kBarDQDrained + 1;
+  static constexpr int kBarDQDrained = kBarDQFull + 1;  // 2: one per 64-column half of dQ
+  static constexpr int kBarDSFree = kBarDQDrained + 2;
   static constexpr int kBarAccDone = kBarDSFree + 1;
   static constexpr int kBarEpi = kBarAccDone + 1;   // 2: one per column half
   static constexpr int kBarDrain = kBarEpi + 2;
@@ -272,12 +274,14 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
       mbar_init(bar(L::kBarQEmpty + s), kRowThreads + 1);  // key-row warps + MMA commit
     }
     mbar_init(bar(L::kBarSFull), 1);
-    mbar_init(bar(L::kBarDPFull), 1);
+    mbar_init(bar(L::kBarDPFull + 0), 1);
+    mbar_init(bar(L::kBarDPFull + 1), 1);
     mbar_init(bar(L::kBarPReady), kRowThreads);
     mbar_init(bar(L::kBarDSReady), kRowThreads);
     mbar_init(bar(L::kBarDVDone), 1);
     mbar_init(bar(L::kBarDQFull), 1);
-    mbar_init(bar(L::kBarDQDrained), 128);
+    mbar_init(bar(L::kBarDQDrained + 0), 128);
+    mbar_init(bar(L::kBarDQDrained + 1), 128);
     mbar_init(bar(L::kBarDSFree), 1);
     mbar_init(bar(L::kBarAccDone), 1);
     mbar_init(bar(L::kBarEpi + 0), 128);
@@ -362,6 +366,12 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
         mma_commit(bar(L::kBarSFull));
         return true;
       };
+      // D = 128: dP^T in two halves of 64 queries (columns kColDP + 64h), each with its own
+      // signal: key-row warpgroup h reads only its half, and half h starts as soon as the drain
+      // has read the dQ columns it overwrites (4x16x8192x128 causal: 933 -> 944 TFLOP/s).
+      // D = 64: one 128-query product signalling both halves (halves measured 8 % slower:
+      // the narrower products cost more than the earlier start gains).
+      constexpr uint32_t kIdDPh = idesc_bf16_f32(128, 64, 0, 0);
       auto issue_dp = [&](int it) {
         const int st = it % NS;
         tc_fence_after_sync();
@@ -371,10 +381,29 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
           mma_ss(tmem + L::kColDP, sdesc_sw128(sV + off, 16, 1024), sdesc_sw128(sdO(st) + off, 16, 1024),
                  kIdSq, kk > 0 ? 1u : 0u);
         }
-        mma_commit(bar(L::kBarDPFull));
+        mma_commit(bar(L::kBarDPFull + 0));
+        mma_commit(bar(L::kBarDPFull + 1));
+      };
+      auto issue_dp_half = [&](int it, int h) {
+        const int st = it % NS;
+        tc_fence_after_sync();
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * (kTile * 128) + (kk & 3) * 32;
+          mma_ss(tmem + L::kColDP + 64 * h, sdesc_sw128(sV + off, 16, 1024),
+                 sdesc_sw128(sdO(st) + off + h * (64 * 128), 16, 1024), kIdDPh, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(bar(L::kBarDPFull + h));
       };
       bool ok = mbar_wait(bar(L::kBarKV), 0, wc) && issue_s(0);
-      if (ok) issue_dp(0);
+      if (ok) {
+        if constexpr (D == 64) {
+          issue_dp(0);
+        } else {
+          issue_dp_half(0, 0);
+          issue_dp_half(0, 1);
+        }
+      }
       for (int it = 0; ok && it < n_it; ++it) {
         const int st = it % NS;
         const uint32_t ph = it & 1;
@@ -414,10 +443,17 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
         }
         mma_commit(bar(L::kBarDSFree));
         mma_commit(bar(L::kBarQEmpty + st));
-        // dP_{i+1} overwrites the dQ_i tile: wait until the drain warps have read it.
+        // dP_{i+1} overwrites the dQ_i tile: each product waits until the drain warps have
+        // read the dQ columns under it.
         if (it + 1 < n_it) {
-          if (!mbar_wait(bar(L::kBarDQDrained), ph, wc)) { ok = false; break; }
-          issue_dp(it + 1);
+          if (!mbar_wait(bar(L::kBarDQDrained + 0), ph, wc)) { ok = false; break; }
+          if constexpr (D == 64) {
+            issue_dp(it + 1);
+          } else {
+            issue_dp_half(it + 1, 0);
+            if (!mbar_wait(bar(L::kBarDQDrained + 1), ph, wc)) { ok = false; break; }
+            issue_dp_half(it + 1, 1);
+          }
         }
       }
       if (ok) mma_commit(bar(L::kBarAccDone));
@@ -511,7 +547,7 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
       tc_fence_before_sync();
       mbar_arrive(bar(L::kBarPReady));
       // phase 2: dS^T = P^T (dP^T - D)
-      bool got = mbar_wait(bar(L::kBarDPFull), ph, wc);
+      bool got = mbar_wait(bar(L::kBarDPFull + half), ph, wc);
       if (it > 0) got = got && mbar_wait(bar(L::kBarDSFree), ph ^ 1, wc);
       if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
       tc_fence_after_sync();
@@ -613,10 +649,9 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
         uint32_t a[32], b[32];
         tmem_ld32(tmem + lane_off + L::kColDP + 64 * h, a);
         tmem_ld32(tmem + lane_off + L::kColDP + 64 * h + 32, b);
-        if (h == D / 64 - 1) {  // every column of this dQ tile is in registers
-          tc_fence_before_sync();
-          mbar_arrive(bar(L::kBarDQDrained));
-        }
+        // these 64 columns are in registers: the dP half over them may be written
+        tc_fence_before_sync();
+        mbar_arrive(bar(L::kBarDQDrained + h));
         if (live) {
 #pragma unroll
           for (int g = 0; g < 8; ++g) {
