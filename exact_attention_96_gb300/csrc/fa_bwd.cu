@@ -182,13 +182,14 @@ struct BwdLayout {
   static constexpr int kBarQFull = 1;
   static constexpr int kBarQEmpty = kBarQFull + NS;
   static constexpr int kBarSFull = kBarQEmpty + NS;
-  static constexpr int kBarDPFull = kBarSFull + 1;    // 2: one per query half
-  static constexpr int kBarPReady = kBarDPFull + 2;
+  static constexpr int kHalves = D == 64 ? 1 : 2;  // dP products (one per query half at D = 128)
+  static constexpr int kBarDPFull = kBarSFull + 1;    // kHalves
+  static constexpr int kBarPReady = kBarDPFull + kHalves;
   static constexpr int kBarDSReady = kBarPReady + 1;
   static constexpr int kBarDVDone = kBarDSReady + 1;
   static constexpr int kBarDQFull = kBarDVDone + 1;
-  static constexpr int kBarDQDrained = kBarDQFull + 1;  // 2: one per 64-column half of dQ
-  static constexpr int kBarDSFree = kBarDQDrained + 2;
+  static constexpr int kBarDQDrained = kBarDQFull + 1;  // kHalves: one per 64-column half of dQ
+  static constexpr int kBarDSFree = kBarDQDrained + kHalves;
   static constexpr int kBarAccDone = kBarDSFree + 1;
   static constexpr int kBarEpi = kBarAccDone + 1;   // 2: one per column half
   static constexpr int kBarDrain = kBarEpi + 2;
@@ -274,14 +275,12 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
       mbar_init(bar(L::kBarQEmpty + s), kRowThreads + 1);  // key-row warps + MMA commit
     }
     mbar_init(bar(L::kBarSFull), 1);
-    mbar_init(bar(L::kBarDPFull + 0), 1);
-    mbar_init(bar(L::kBarDPFull + 1), 1);
+    for (int h = 0; h < L::kHalves; ++h) mbar_init(bar(L::kBarDPFull + h), 1);
     mbar_init(bar(L::kBarPReady), kRowThreads);
     mbar_init(bar(L::kBarDSReady), kRowThreads);
     mbar_init(bar(L::kBarDVDone), 1);
     mbar_init(bar(L::kBarDQFull), 1);
-    mbar_init(bar(L::kBarDQDrained + 0), 128);
-    mbar_init(bar(L::kBarDQDrained + 1), 128);
+    for (int h = 0; h < L::kHalves; ++h) mbar_init(bar(L::kBarDQDrained + h), 128);
     mbar_init(bar(L::kBarDSFree), 1);
     mbar_init(bar(L::kBarAccDone), 1);
     mbar_init(bar(L::kBarEpi + 0), 128);
@@ -369,7 +368,7 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
       // D = 128: dP^T in two halves of 64 queries (columns kColDP + 64h), each with its own
       // signal: key-row warpgroup h reads only its half, and half h starts as soon as the drain
       // has read the dQ columns it overwrites (4x16x8192x128 causal: 933 -> 944 TFLOP/s).
-      // D = 64: one 128-query product signalling both halves (halves measured 8 % slower:
+      // D = 64: one 128-query product read by both warpgroups (halves measured 8 % slower:
       // the narrower products cost more than the earlier start gains).
       constexpr uint32_t kIdDPh = idesc_bf16_f32(128, 64, 0, 0);
       auto issue_dp = [&](int it) {
@@ -381,8 +380,7 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
           mma_ss(tmem + L::kColDP, sdesc_sw128(sV + off, 16, 1024), sdesc_sw128(sdO(st) + off, 16, 1024),
                  kIdSq, kk > 0 ? 1u : 0u);
         }
-        mma_commit(bar(L::kBarDPFull + 0));
-        mma_commit(bar(L::kBarDPFull + 1));
+        mma_commit(bar(L::kBarDPFull));
       };
       auto issue_dp_half = [&](int it, int h) {
         const int st = it % NS;
@@ -547,7 +545,7 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
       tc_fence_before_sync();
       mbar_arrive(bar(L::kBarPReady));
       // phase 2: dS^T = P^T (dP^T - D)
-      bool got = mbar_wait(bar(L::kBarDPFull + half), ph, wc);
+      bool got = mbar_wait(bar(L::kBarDPFull + (L::kHalves > 1 ? half : 0)), ph, wc);
       if (it > 0) got = got && mbar_wait(bar(L::kBarDSFree), ph ^ 1, wc);
       if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
       tc_fence_after_sync();
