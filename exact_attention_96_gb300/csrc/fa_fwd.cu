@@ -173,7 +173,13 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
       for (int j = 0; j < nkv; ++j) {
         const int st = j % NS;
         const uint32_t ph = (j / NS) & 1;
-        if (j >= NS && !mbar_wait(bar(L::kBarKEmpty + st), ph ^ 1, wc)) { ok = false; break; }
+        // With two stages the stage and the S buffer of a tile coincide, and S_{j-2} landing
+        // means K_{j-2} has been read: wait on the S barrier and spare the MMA thread a commit
+        // (the barrier cannot run a phase ahead: S_j needs the K_j loaded below).
+        if (j >= NS && !mbar_wait(bar((NS == 2 ? L::kBarSFull : L::kBarKEmpty) + st), ph ^ 1, wc)) {
+          ok = false;
+          break;
+        }
         if (j != args.withhold_k_tile) {  // the test hook leaves this tile's barrier unarmed
           mbar_arrive_expect_tx(bar(L::kBarKFull + st), L::kKVBytes);
           for (int s = 0; s < L::kSlabs; ++s)
@@ -219,7 +225,7 @@ fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
           const uint64_t b = sdesc_sw128(sK(st) + (kk >> 2) * (BC * 128) + (kk & 3) * 32, 16, 1024);
           mma_ss(d_tmem, a, b, kIdS, kk > 0 ? 1u : 0u);
         }
-        mma_commit(bar(L::kBarKEmpty + st));
+        if constexpr (NS != 2) mma_commit(bar(L::kBarKEmpty + st));
         mma_commit(bar(L::kBarSFull + (jj & 1)));
         return true;
       };
