@@ -47,7 +47,7 @@ struct L256 {
   static constexpr int kBarOff = kDOff + kQ * 4;
   enum {
     kBarKV, kBarQFull, kBarQEmpty, kBarOFull, kBarOEmpty, kBarSFull, kBarDPFull, kBarPReady,
-    kBarDSReady, kBarDVDone, kBarDQFull, kBarDQDrained, kBarDSFree, kBarAccDone, kBarEpi0,
+    kBarDSReady, kBarDQFull, kBarDQDrained, kBarAccDone, kBarEpi0,
     kBarEpi1, kBarDrain, kNumBars
   };
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
@@ -99,10 +99,8 @@ fa_bwd_d256_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
     mbar_init(bar(L::kBarDPFull), 1);
     mbar_init(bar(L::kBarPReady), kRowThreads);
     mbar_init(bar(L::kBarDSReady), kRowThreads);
-    mbar_init(bar(L::kBarDVDone), 1);
     mbar_init(bar(L::kBarDQFull), 1);
     mbar_init(bar(L::kBarDQDrained), 128);
-    mbar_init(bar(L::kBarDSFree), 1);
     mbar_init(bar(L::kBarAccDone), 1);
     mbar_init(bar(L::kBarEpi0), 128);
     mbar_init(bar(L::kBarEpi1), 128);
@@ -193,7 +191,8 @@ fa_bwd_d256_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                  sdesc_sw128(sdO + (2 * z) * (kQ * 128) + kk * (16 * 128), kQ * 128, 1024), kIdAcc,
                  (it > 0 || kk > 0) ? 1u : 0u);
         }
-        mma_commit(bar(L::kBarDVDone));
+        // one commit serves both: dO_i's stage (with the key rows' arrivals) and, for the
+        // S_{i+1} issue below, the end of dV_i (see there)
         mma_commit(bar(L::kBarOEmpty));
         if (!mbar_wait(bar(L::kBarDSReady), ph, wc)) { ok = false; break; }
         tc_fence_after_sync();
@@ -213,11 +212,14 @@ fa_bwd_d256_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                  sdesc_sw128(sK + (2 * z) * (kKeys * 128) + kk * (16 * 128), kKeys * 128, 1024),
                  sdesc_sw128(sdS + kk * (16 * 128), kQ * 128, 1024), kIdDQ, kk > 0 ? 1u : 0u);
         }
-        mma_commit(bar(L::kBarDQFull));
-        mma_commit(bar(L::kBarDSFree));
+        mma_commit(bar(L::kBarDQFull));  // also frees dS^T_i (dQ^T_i is its last reader)
         if (it + 1 < n_it) {
-          // S_{i+1} overwrites P^T_i (read by dV_i and by the key rows before dS_i was published)
-          if (!mbar_wait(bar(L::kBarDVDone), ph, wc) || !mbar_wait(bar(L::kBarQFull), (it + 1) & 1, wc)) {
+          // S_{i+1} overwrites P^T_i (read by dV_i and by the key rows before dS_i was published).
+          // dV_i has completed once the dO stage's empty barrier has: the key rows arrived on it
+          // after publishing dS_i, which dQ^T_i above already waited for, so this wait is on
+          // dV_i alone; the barrier cannot run a phase ahead (its next completion needs the key
+          // rows' arrival for tile i+1, after dP_{i+1} is issued below).
+          if (!mbar_wait(bar(L::kBarOEmpty), ph, wc) || !mbar_wait(bar(L::kBarQFull), (it + 1) & 1, wc)) {
             ok = false;
             break;
           }
@@ -276,7 +278,9 @@ fa_bwd_d256_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
       mbar_arrive(bar(L::kBarPReady));
       mbar_arrive(bar(L::kBarQEmpty));   // done with this tile's LSE
       bool got = mbar_wait(bar(L::kBarDPFull), ph, wc);
-      if (it > 0) got = got && mbar_wait(bar(L::kBarDSFree), ph ^ 1, wc);
+      // dS^T_{i-1} is free once dQ^T_{i-1} (its last reader) has completed; that barrier's
+      // next completion needs this tile's dS, so it cannot run a phase ahead
+      if (it > 0) got = got && mbar_wait(bar(L::kBarDQFull), ph ^ 1, wc);
       if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
       tc_fence_after_sync();
       {
