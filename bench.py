@@ -309,17 +309,19 @@ SWEEP_DROPOUT = [  # (name, B, H, N, d, causal, p): forward and backward with dr
 
 
 def timed(fn, reps):
+    """Median milliseconds of `reps` calls, each bracketed by CUDA events on the current
+    stream, after 5 warm-up calls."""
     import torch
-    for _ in range(3):
+    for _ in range(5):
         fn()
     torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(reps):
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    for e0, e1 in ev:
+        e0.record()
         fn()
-    e1.record()
+        e1.record()
     torch.cuda.synchronize()
-    return e0.elapsed_time(e1) / reps
+    return statistics.median(e0.elapsed_time(e1) for e0, e1 in ev)
 
 
 def naive_peak_bytes(q, k, v, do, scale):
@@ -362,16 +364,7 @@ def run_sweep(reps: int = 20):
                  "bwd": lambda: fa.backward(q, k, v, o, do, lse, causal=causal, scale=scale,
                                             workspace=ws, grads=grads)}
         for ps in passes:
-            for _ in range(3):
-                calls[ps]()
-            torch.cuda.synchronize()
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record()
-            for _ in range(reps):
-                calls[ps]()
-            e1.record()
-            torch.cuda.synchronize()
-            ms = e0.elapsed_time(e1) / reps
+            ms = timed(calls[ps], reps if N < 65536 else max(5, reps // 4))
             flops = fwd_f if ps == "fwd" else bwd_f
             tf = flops / (ms * 1e-3) / 1e12
             line = {"config": name, "shape": [B, H, N, d], "causal": causal, "pass": ps, "ms": ms,
@@ -449,16 +442,7 @@ def run_sweep(reps: int = 20):
                 for s in (2, 3))
         o, lse = fa.forward_splitkv(q, k, v)
         ws = torch.empty(abi.fa_fwd_splitkv_workspace_bytes(B, H, Nq, Nk, d, 0), dtype=torch.uint8, device="cuda")
-        for _ in range(3):
-            fa.forward_splitkv(q, k, v, out=o, lse=lse, workspace=ws)
-        torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record()
-        for _ in range(reps):
-            fa.forward_splitkv(q, k, v, out=o, lse=lse, workspace=ws)
-        e1.record()
-        torch.cuda.synchronize()
-        ms = e0.elapsed_time(e1) / reps
+        ms = timed(lambda: fa.forward_splitkv(q, k, v, out=o, lse=lse, workspace=ws), reps)
         nbytes = 2.0 * B * H * Nk * d * 2 + 2.0 * B * H * Nq * d * 2 + 4.0 * B * H * Nq
         print(json.dumps({"config": name, "shape": [B, H, Nq, Nk, d], "pass": "fwd-splitkv", "ms": ms,
                           "alg_gbs": nbytes / (ms * 1e-3) / 1e9, "frac_hbm": nbytes / (ms * 1e-3) / 1e9 / hbm,
