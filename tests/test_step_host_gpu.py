@@ -34,6 +34,8 @@ def host_bf16(bits):
     (1, 4, 513, 128, False, 3),   # N % 4 != 0: chunks rounded to 4 heads (one chunk)
     (4, 16, 1024, 128, True, 7),  # 64 heads in 7 chunks
     (1, 2, 256, 256, True, 1),
+    (4, 16, 2048, 64, True, 0),   # default plan: 15 heads per chunk (1.5 waves of tiles), 15*4+4
+    (4, 16, 2047, 64, False, 0),  # default plan, N % 4 != 0: 16 heads per chunk, 4-head aligned
 ])
 def test_step_host_matches_device_calls(B, H, N, d, causal, chunks):
     host = I.attention_inputs(B, H, N, d, seed=N + d)
