@@ -433,7 +433,6 @@ fa_status fa_bwd_dropout(const void* q, const void* k, const void* v, const void
   fa::DropoutParams dp;
   const fa_status st = make_dropout(dropout_p, seed, &dp);
   if (st != FA_OK) return st;
-  if (d == 256) return FA_ERR_UNSUPPORTED;
   return bwd_impl(q, k, v, o, dout, lse, dq, dk, dv, B, H, N, d, scale, causal, &dp, workspace,
                   workspace_bytes, stream);
 }

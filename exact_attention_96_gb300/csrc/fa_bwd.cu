@@ -207,34 +207,6 @@ struct BwdLayout {
   static_assert(kBytes <= 232448, "shared memory budget");
 };
 
-// Keep bits of key `key` for queries qb .. qb+63 (bit c of the result = query qb + c).  All 32
-// lanes of the warp take part (shuffles); lane & 7 must equal key & 7.
-__device__ __forceinline__ uint64_t dropout_key_bits64(const DropoutParams& dp, int key, int qb, int bh, int lane) {
-  const uint32_t u = uint32_t(lane & 7);
-  const uint32_t g = uint32_t(key) >> 3;
-  uint64_t out = 0;
-#pragma unroll
-  for (int b = 0; b < 8; b += 2) {
-#pragma unroll
-    for (int bb = 0; bb < 2; ++bb) {
-      // row u of this octet's 8 x 8 bit block: keep bits of keys 8g .. 8g+7 for query 8(b+bb) + u
-      const uint32_t row = dropout_keep8(dp, g, uint32_t(qb + 8 * (b + bb)) + u, uint32_t(bh));
-      uint32_t x = row << (8 * (u & 3));
-      x |= __shfl_xor_sync(0xffffffffu, x, 1);
-      x |= __shfl_xor_sync(0xffffffffu, x, 2);  // rows of this quad of lanes
-      const uint32_t y = __shfl_xor_sync(0xffffffffu, x, 4);
-      const uint32_t lo = u < 4 ? x : y;      // rows 0-3, one per byte
-      const uint32_t hi = u < 4 ? y : x;      // rows 4-7
-      // column u: bit u of every byte, gathered into a nibble (the four products land on
-      // distinct bits 24..27, so no carries)
-      const uint32_t nlo = (((lo >> u) & 0x01010101u) * 0x01020408u) >> 24;
-      const uint32_t nhi = (((hi >> u) & 0x01010101u) * 0x01020408u) >> 24;
-      out |= uint64_t(nlo | (nhi << 4)) << (8 * (b + bb));
-    }
-  }
-  return out;
-}
-
 template <int D, int NS, bool CAUSAL, bool DROPOUT>
 __global__ void __launch_bounds__(kMainThreads, 1)
 fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -482,7 +454,7 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
       const float* dvv = reinterpret_cast<const float*>(smem + L::kDOff + st * 512) + c0;
       uint32_t km[2] = {0u, 0u};  // dropout keep bits: bit c % 32 of word c / 32 = query q0 + c0 + c
       if constexpr (DROPOUT) {
-        const uint64_t bits = dropout_key_bits64(args.dropout, key, q0 + c0, bh, lane);
+        const uint64_t bits = dropout_key_bits<8>(args.dropout, key, q0 + c0, bh, lane);
         km[0] = uint32_t(bits);
         km[1] = uint32_t(bits >> 32);
         // keep the generator work here, ahead of the S^T wait, instead of letting it sink into
@@ -725,9 +697,8 @@ cudaError_t launch_bwd_all(const BwdMaps& m, const CUtensorMap& lse2, const CUte
       if (e != cudaSuccess) return e;
       return launch_prep_and_convert<128>(a, Np, n_q_tiles, s, false);
     case 256:
-      if (dropout) return cudaErrorNotSupported;
       if ((e = launch_prep_and_convert<256>(a, Np, n_q_tiles, s, true)) != cudaSuccess) return e;
-      e = launch_bwd_main_d256(m.q64, m.k, m.v, m.dout64, m.lse2_64, m.dvec_64, dk, dv, a, causal, s);
+      e = launch_bwd_main_d256(m.q64, m.k, m.v, m.dout64, m.lse2_64, m.dvec_64, dk, dv, a, causal, s, dropout);
       if (e != cudaSuccess) return e;
       return launch_prep_and_convert<256>(a, Np, n_q_tiles, s, false);
     default:

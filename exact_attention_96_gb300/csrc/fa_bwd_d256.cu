@@ -15,6 +15,11 @@
 // dS^T [128 x 64] (16 KB), LSE*log2e and D tiles.
 // Roles: warps 0-7 key rows (two warpgroups split the 64 query columns), warps 8-11 dQ
 // drain, warp 12 TMA producer, warp 13 TMEM + MMA issuer.
+// Dropout (template flag): as in the d <= 128 kernel, with Z = keep * scale_keep,
+// dV = (P * Z)^T dO and dS = P * (dP * Z - D); a key row draws the keep bits of its key for
+// its 32 queries by the shared octet scheme, writes P^T * keep for the dV product where the
+// plain kernel writes P^T, and the unmasked P^T in the next 16 columns of its S^T range (read
+// back for dS).
 
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -57,7 +62,7 @@ struct L256 {
   static_assert(kBytes <= 232448, "shared memory budget");
 };
 
-template <bool CAUSAL>
+template <bool CAUSAL, bool DROPOUT>
 __global__ void __launch_bounds__(kThreads, 1)
 fa_bwd_d256_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
@@ -251,6 +256,11 @@ fa_bwd_d256_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
       const uint32_t ph = it & 1;
       const int q0 = (it_first + it) * kQ;
       const bool edge = (CAUSAL && q0 < k0 + kKeys) || (q0 + kQ > N);
+      uint32_t km = 0u;  // dropout keep bits: bit c = query q0 + c0 + c
+      if constexpr (DROPOUT) {
+        km = uint32_t(dropout_key_bits<4>(args.dropout, key, q0 + c0, bh, lane));
+        asm volatile("" : "+r"(km));  // generator work ahead of the S^T wait
+      }
       if (!__all_sync(0xffffffffu, mbar_wait(bar(L::kBarSFull), ph, wc))) { ok = false; break; }
       tc_fence_after_sync();
       {
@@ -271,6 +281,15 @@ fa_bwd_d256_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
           }
           w[e / 2] = pack_bf16x2(p0, p1);
         }
+        if constexpr (DROPOUT) {
+          // unmasked P^T for dS in the second 16 columns; P^T * keep for the dV product
+          tmem_st16(tmem + lane_off + L::kColS + c0 + 16, w);
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const uint32_t kb = km >> (2 * e);
+            w[e] &= ((kb & 1u) ? 0x0000FFFFu : 0u) | ((kb & 2u) ? 0xFFFF0000u : 0u);
+          }
+        }
         tmem_st16(tmem + lane_off + L::kColS + c0, w);
       }
       tmem_wait_st();
@@ -287,15 +306,20 @@ fa_bwd_d256_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
         uint32_t r[32];
         uint32_t pr[16];
         tmem_ld32(tmem + lane_off + L::kColDP + c0, r);
-        tmem_ld16(tmem + lane_off + L::kColS + c0, pr);
+        tmem_ld16(tmem + lane_off + L::kColS + c0 + (DROPOUT ? 16 : 0), pr);
         uint32_t w[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
           const float p0 = __uint_as_float(pr[e / 2] << 16);
           const float p1 = __uint_as_float(pr[e / 2] & 0xFFFF0000u);
+          float dp0 = __uint_as_float(r[e]), dp1 = __uint_as_float(r[e + 1]);
+          if constexpr (DROPOUT) {
+            const uint32_t kb = km >> e;
+            dp0 = (kb & 1u) ? dp0 * args.dropout.scale : 0.f;
+            dp1 = (kb & 2u) ? dp1 * args.dropout.scale : 0.f;
+          }
           // dvv holds -D: dS = P (dP - D) two at a time
-          const float2 ds = fmul2(make_float2(p0, p1), fadd2(make_float2(__uint_as_float(r[e]), __uint_as_float(r[e + 1])),
-                                                             make_float2(dvv[e], dvv[e + 1])));
+          const float2 ds = fmul2(make_float2(p0, p1), fadd2(make_float2(dp0, dp1), make_float2(dvv[e], dvv[e + 1])));
           float ds0 = ds.x, ds1 = ds.y;
           if (edge) {
             const int qa = q0 + c0 + e;
@@ -319,7 +343,7 @@ fa_bwd_d256_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
     // epilogue: half 0 stores the dV slice, half 1 the dK slice (scaled)
     const bool fin = ok && __all_sync(0xffffffffu, mbar_wait(bar(L::kBarAccDone), 0, wc));
     const uint32_t col = half == 0 ? L::kColDV : L::kColDK;
-    const float mul = half == 0 ? 1.f : args.scale;
+    const float mul = half == 0 ? (DROPOUT ? args.dropout.scale : 1.f) : args.scale;
     uint8_t* stage = smem + (half == 0 ? L::kQOff : L::kdOOff);   // 2 slabs of [128 x 128 B]
     if (fin) {
       tc_fence_after_sync();
@@ -387,8 +411,9 @@ fa_bwd_d256_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
 cudaError_t launch_bwd_main_d256(const CUtensorMap& q64, const CUtensorMap& k, const CUtensorMap& v,
                                  const CUtensorMap& dout64, const CUtensorMap& lse2_64,
                                  const CUtensorMap& d64, const CUtensorMap& dk, const CUtensorMap& dv,
-                                 const BwdArgs& a, bool causal, cudaStream_t s) {
-  auto kern = causal ? fa_bwd_d256_kernel<true> : fa_bwd_d256_kernel<false>;
+                                 const BwdArgs& a, bool causal, cudaStream_t s, bool dropout) {
+  auto kern = dropout ? (causal ? fa_bwd_d256_kernel<true, true> : fa_bwd_d256_kernel<false, true>)
+                      : (causal ? fa_bwd_d256_kernel<true, false> : fa_bwd_d256_kernel<false, false>);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L256::kBytes);
   if (e != cudaSuccess) return e;
   dim3 grid((a.N + kKeys - 1) / kKeys, a.BH, 2);

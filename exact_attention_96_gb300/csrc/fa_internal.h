@@ -103,16 +103,17 @@ struct BwdMaps {
   CUtensorMap q64, dout64, lse2_64, dvec_64;
 };
 
-// Backward main kernel for d = 256 (fa_bwd_d256.cu).
+// Backward main kernel for d = 256 (fa_bwd_d256.cu); with `dropout` it applies the mask of
+// a.dropout.
 cudaError_t launch_bwd_main_d256(const CUtensorMap& q64, const CUtensorMap& k, const CUtensorMap& v,
                                  const CUtensorMap& dout64, const CUtensorMap& lse2_64,
                                  const CUtensorMap& d64, const CUtensorMap& dk, const CUtensorMap& dv,
-                                 const BwdArgs& a, bool causal, cudaStream_t s);
+                                 const BwdArgs& a, bool causal, cudaStream_t s, bool dropout);
 
 // Backward: prep, main and dQ-convert launches.  `lse2` and `dvec` describe the fp32
 // [B*H, Np] rows of the workspace (box 128 x 1 x 1); `dk`, `dv` the bf16 outputs.
 // Np = N rounded up to a multiple of 4.
-// With `dropout` (d <= 128 only) the main kernel applies the mask of a.dropout.
+// With `dropout` the main kernel applies the mask of a.dropout.
 cudaError_t launch_bwd_all(const BwdMaps& m, const CUtensorMap& lse2, const CUtensorMap& dvec,
                            const CUtensorMap& dk, const CUtensorMap& dv, const BwdArgs& a,
                            bool causal, int Np, cudaStream_t s, bool dropout = false);

@@ -54,4 +54,38 @@ __device__ __forceinline__ uint32_t dropout_keep8(const DropoutParams& dp, uint3
   return two(w.x) | (two(w.y) << 2) | (two(w.z) << 4) | (two(w.w) << 6);
 }
 
+// Keep bits of key `key` for queries qb .. qb + 8 kOctets - 1 (bit c of the result = query
+// qb + c), for a thread that owns one key row.  The eight lanes holding keys 8g .. 8g+7 share
+// the generator calls: lane u draws the call of query 8b + u (8 bits, one per key), the octet
+// exchanges its 8 x 8 bit block by shuffles and each lane gathers its own bit column -- one
+// call per lane per 8 queries.  All 32 lanes of the warp take part; lane & 7 must equal
+// key & 7.
+template <int kOctets>
+__device__ __forceinline__ uint64_t dropout_key_bits(const DropoutParams& dp, int key, int qb, int bh, int lane) {
+  static_assert(kOctets % 2 == 0 && kOctets <= 8, "up to 64 queries, in pairs of octets");
+  const uint32_t u = uint32_t(lane & 7);
+  const uint32_t g = uint32_t(key) >> 3;
+  uint64_t out = 0;
+#pragma unroll
+  for (int b = 0; b < kOctets; b += 2) {
+#pragma unroll
+    for (int bb = 0; bb < 2; ++bb) {
+      // row u of this octet's 8 x 8 bit block: keep bits of keys 8g .. 8g+7 for query 8(b+bb) + u
+      const uint32_t row = dropout_keep8(dp, g, uint32_t(qb + 8 * (b + bb)) + u, uint32_t(bh));
+      uint32_t x = row << (8 * (u & 3));
+      x |= __shfl_xor_sync(0xffffffffu, x, 1);
+      x |= __shfl_xor_sync(0xffffffffu, x, 2);  // rows of this quad of lanes
+      const uint32_t y = __shfl_xor_sync(0xffffffffu, x, 4);
+      const uint32_t lo = u < 4 ? x : y;      // rows 0-3, one per byte
+      const uint32_t hi = u < 4 ? y : x;      // rows 4-7
+      // column u: bit u of every byte, gathered into a nibble (the four products land on
+      // distinct bits 24..27, so no carries)
+      const uint32_t nlo = (((lo >> u) & 0x01010101u) * 0x01020408u) >> 24;
+      const uint32_t nhi = (((hi >> u) & 0x01010101u) * 0x01020408u) >> 24;
+      out |= uint64_t(nlo | (nhi << 4)) << (8 * (b + bb));
+    }
+  }
+  return out;
+}
+
 }  // namespace fa

@@ -20,7 +20,7 @@
  *    (the library frees nothing it did not allocate).  Layout is contiguous row-major
  *    [B, H, N, d] with d innermost for Q, K, V, O, dO, dQ, dK, dV (bfloat16) and [B, H, N]
  *    for LSE and D (float32).  Every pointer must be 16-byte aligned.
- *  - Sizes.  B >= 1, H >= 1, N >= 1, B*H <= 65535 * 65535, N <= 2^20; d in {64, 128, 256}.
+ *  - Sizes.  B >= 1, H >= 1, N >= 1, B*H <= 65535, N <= 2^20; d in {64, 128, 256}.
  *  - Asynchrony.  Work is enqueued on `stream` (0 = legacy default stream) and the call
  *    returns without synchronising.  A device-side failure (a bounded wait that gave
  *    up) is recorded in a per-device error word and reported by fa_status_check().
@@ -154,7 +154,7 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
  *   dropout_p: in [0, 1), else FA_ERR_INVALID_ARG.  seed: any 64-bit value.
  * fa_fwd_dropout takes fa_fwd's arguments plus (dropout_p, seed); fa_bwd_dropout takes
  * fa_bwd's plus the same pair, which must be those of the forward call (with lse and o from
- * it).  fa_bwd_dropout with d = 256 returns FA_ERR_UNSUPPORTED.
+ * it).
  */
 fa_status fa_fwd_dropout(const void* q, const void* k, const void* v, void* o, float* lse,
                          int B, int H, int N, int d, float scale, int causal,

@@ -140,8 +140,8 @@ def test_dropout_probability_is_validated(lib, p):
 
 
 def test_dropout_argument_checks_before_launch(lib):
-    # the backward dropout path exists for d <= 128 only
-    assert abi.fa_bwd_dropout(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 128, 256, 0.125, 0,
+    # the backward dropout path takes the plain path's head dims
+    assert abi.fa_bwd_dropout(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 128, 96, 0.125, 0,
                               0.1, 1, FAKE, 1 << 30, None) == abi.FA_ERR_UNSUPPORTED
     # the usual size, pointer and alignment checks still come first
     assert abi.fa_fwd_dropout(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 0, 64, 0.125, 0, 0.1, 1, None) == \

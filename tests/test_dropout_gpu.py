@@ -59,7 +59,7 @@ def test_forward_mask_bit_exact(causal, p, seed):
         assert np.array_equal(got, keep[..., t:t + n]), (t, np.argwhere(got != keep[..., t:t + n])[:5])
 
 
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [64, 128, 256])
 @pytest.mark.parametrize("causal", [False, True])
 def test_backward_mask_bit_exact(d, causal):
     B, H, N, p, seed = 1, 3, 700, 0.4, 424242
@@ -132,6 +132,8 @@ BWD = [
     (1, 2, 383, 64, False, 0.3),
     (2, 4, 1024, 128, True, 0.1),
     (3, 3, 260, 64, True, 0.2),  # causal heads in a full group of eight and a partial one
+    (1, 2, 300, 256, True, 0.2),
+    (2, 1, 200, 256, False, 0.3),
 ]
 
 
@@ -173,12 +175,3 @@ def test_same_seed_repeats_and_new_seed_changes():
     b = fa.forward(q, k, v, dropout_p=0.2, seed=11)[0]
     c = fa.forward(q, k, v, dropout_p=0.2, seed=12)[0]
     assert torch.equal(a, b) and not torch.equal(a, c)
-
-
-def test_backward_head_dim_256_is_unsupported():
-    B, H, N, d = 1, 1, 128, 256
-    q, k, v, do = (to_device(x) for x in I.attention_inputs(B, H, N, d, seed=9))
-    o, lse = fa.forward(q, k, v, dropout_p=0.1, seed=1)
-    with pytest.raises(abi.FAError) as e:
-        fa.backward(q, k, v, o, do, lse, dropout_p=0.1, seed=1)
-    assert e.value.status == abi.FA_ERR_UNSUPPORTED
