@@ -79,9 +79,14 @@ fa_bwd_d256_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
   uint8_t* smem = smem_raw;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const RankHead rh = CAUSAL ? causal_dispatch_order() : RankHead{int(blockIdx.x), int(blockIdx.y)};
+  // The two head-dimension slices of a key tile are dispatched next to each other, so that
+  // they stream the same Q and dO tiles at about the same time and share them in L2.
+  const int tiles = int(gridDim.x), heads = int(gridDim.y);
+  const int lin = int(blockIdx.x) + tiles * (int(blockIdx.y) + heads * int(blockIdx.z));
+  const int z = lin & 1;                  // d slice [128z, 128z + 128)
+  const int pair = lin >> 1;              // (key tile, head) pair
+  const RankHead rh = CAUSAL ? causal_order_of(pair, tiles, heads) : RankHead{pair % tiles, pair / tiles};
   const int bh = rh.bh;
-  const int z = blockIdx.z;               // d slice [128z, 128z + 128)
   const int k0 = rh.rank * kKeys;         // causal: key tile 0 is the heaviest
   const int N = args.N;
   const int n_qt = (N + kQ - 1) / kQ;     // 64-row query tiles

@@ -24,13 +24,14 @@ constexpr int kCausalGroup = 8;
 struct RankHead {
   int rank, bh;
 };
-__device__ __forceinline__ RankHead causal_dispatch_order() {
-  const int tiles = int(gridDim.x), heads = int(gridDim.y);
-  const int l = int(blockIdx.x) + tiles * int(blockIdx.y);
+__device__ __forceinline__ RankHead causal_order_of(int l, int tiles, int heads) {
   const int g0 = l / (kCausalGroup * tiles) * kCausalGroup;
   const int gs = min(kCausalGroup, heads - g0);
   const int r = l - g0 * tiles;
   return {r / gs, g0 + r % gs};
+}
+__device__ __forceinline__ RankHead causal_dispatch_order() {
+  return causal_order_of(int(blockIdx.x) + int(gridDim.x) * int(blockIdx.y), int(gridDim.x), int(gridDim.y));
 }
 #endif
 
