@@ -18,8 +18,11 @@ namespace fa {
 // alone.  Instead the heads are taken in groups of kCausalGroup, and inside a group every
 // head's rank-r CTA is dispatched before any rank-(r + 1) CTA: the heavy CTAs start first,
 // and the few heads in flight still share their streamed tiles (and the dQ accumulator) in
-// L2.  Maps the CTA's linear index in the (gridDim.x = tiles, gridDim.y = heads) grid to its
-// (rank, head); a bijection for any sizes.
+// L2.  causal_order_of maps a linear index l in [0, tiles * heads) to a (rank, head), a
+// bijection for any sizes; causal_dispatch_order applies it to the CTA's index in a
+// (gridDim.x = tiles, gridDim.y = heads) grid.  Measured with groups of 2 to 32 heads at
+// 4x16x8192x128 causal: 8 is best (larger groups spread the streamed tiles over more heads
+// than L2 holds).
 constexpr int kCausalGroup = 8;
 struct RankHead {
   int rank, bh;
