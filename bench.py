@@ -57,29 +57,33 @@ def config_dict(extra=None):
 
 
 class ClockSampler:
-    """nvidia-smi clock / throttle-reason sampling in the background (200 ms period)."""
+    """nvidia-smi clock / throttle-reason sampling in the background (every `period_ms`), each
+    sample stamped, so that a summary can be restricted to a window of host wall-clock time."""
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, device_index: int):
+    def __init__(self, device_index: int, period_ms: int = 20):
         self.device_index = device_index
+        self.period_ms = period_ms
         self.proc = None
+        self.lines = []
 
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.device_index), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", str(self.period_ms)],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
+        time.sleep(0.3)  # let the first samples arrive before the measured work starts
         return self
 
     def __exit__(self, *exc):
-        self.lines = []
         if self.proc is not None:
+            time.sleep(2.5 * self.period_ms / 1000.0)  # the sample that closes the last window
             self.proc.terminate()
             try:
                 out, _ = self.proc.communicate(timeout=5)
@@ -89,23 +93,35 @@ class ClockSampler:
             self.lines = [l for l in out.splitlines() if l.strip()]
         return False
 
-    def summary(self):
-        sm, smax, reasons = [], None, set()
+    def summary(self, t0=None, t1=None):
+        """Median SM clock, maximum clock and the throttle reasons seen in samples stamped
+        within [t0, t1] (datetime, local time as nvidia-smi prints it; None: every sample)."""
+        import datetime as dt
+        sm, smax, reasons, power = [], None, set(), []
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in getattr(self, "lines", []):
+        for line in self.lines:
             parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 9:
+            if len(parts) < 10:
                 continue
             try:
-                sm.append(float(parts[1]))
-                smax = float(parts[2])
+                stamp = dt.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f")
+                clk, cmax = float(parts[2]), float(parts[3])
             except ValueError:
                 continue
-            for name, flag in zip(names, parts[5:9]):
+            if (t0 is not None and stamp < t0) or (t1 is not None and stamp > t1):
+                continue
+            sm.append(clk)
+            smax = cmax
+            try:
+                power.append(float(parts[4]))
+            except ValueError:
+                pass
+            for name, flag in zip(names, parts[6:10]):
                 if flag.lower() == "active":
                     reasons.add(name)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "reasons": sorted(reasons), "samples": len(sm),
+                "power_w_max": max(power) if power else None, "period_ms": self.period_ms}
 
 
 # --------------------------------------------------------------- CPU oracle ----
@@ -135,7 +151,7 @@ def cpu_oracle_sample(target_s: float = 12.0, max_heads: int = 16):
     except Exception:
         cores = os.cpu_count()
     return {"value": (fwd + bwd) / elapsed / 1e12, "unit": "TFLOPS", "cores": cores, "kind": "oracle",
-            "sample": f"{heads} of {w['B'] * w['H']} heads (B=1 slices of the workload), fwd+bwd, "
+            "seconds": elapsed, "sample": f"{heads} of {w['B'] * w['H']} heads (B=1 slices of the workload), fwd+bwd, "
                       f"fp64 numpy, {elapsed:.1f} s"}
 
 
@@ -149,9 +165,14 @@ def run_reference(args, rank, world):
             samples.append(r)
     value = statistics.median(s["value"] for s in samples)
     fwd, bwd = step_flops(**WORKLOAD)
+    heads = WORKLOAD["B"] * WORKLOAD["H"]
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": (fwd + bwd) / (value * 1e12) * 1e3, "higher_is_better": True,
+            # one step = the oracle's forward + backward of one of the workload's heads
+            "ms_per_step": statistics.median(s["seconds"] for s in samples) * 1e3,
+            "step": f"forward + backward of 1 of the {heads} heads (B=1, H=1 slice of the workload)",
+            "ms_full_workload_extrapolated": (fwd + bwd) / (value * 1e12) * 1e3,
+            "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": config_dict(),
             "cpu_baseline": {"kind": "oracle", "cores": samples[-1]["cores"], "value": value,
@@ -219,11 +240,18 @@ def run_gpu(args, rank, world, local_rank):
     if fa.status_check(dev) != abi.FA_OK:
         raise RuntimeError("device status after warm-up is not FA_OK")
 
-    # Device-timed region: events around every call on the launching stream.
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    # Device-timed region: events around every call on the launching stream, and around the
+    # backward's main kernel alone (the library records that pair on the same stream).
+    import ctypes
+    import datetime as dt
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    for e in ev:  # create the events (torch makes them on first record)
+        for x in e:
+            x.record(stream)
     barrier()
     torch.cuda.synchronize(dev)
     with ClockSampler(local_rank) as clocks:
+        t_start = dt.datetime.now()
         start = torch.cuda.Event(enable_timing=True)
         end = torch.cuda.Event(enable_timing=True)
         start.record(stream)
@@ -231,14 +259,31 @@ def run_gpu(args, rank, world, local_rank):
             ev[i][0].record(stream)
             fa.forward(q, k, v, causal=causal, scale=scale, out=o, lse=lse)
             ev[i][1].record(stream)
+            abi.check("fa_profile_next_bwd_main", abi.fa_profile_next_bwd_main(
+                ctypes.c_void_p(ev[i][3].cuda_event), ctypes.c_void_p(ev[i][4].cuda_event)))
             fa.backward(q, k, v, o, do, lse, causal=causal, scale=scale, workspace=ws, grads=(dq, dk, dv))
             ev[i][2].record(stream)
         end.record(stream)
         torch.cuda.synchronize(dev)
+        t_end = dt.datetime.now()
+        barrier()
+        total_ms = start.elapsed_time(end)
+        # The same steps back to back for at least a second more, timed as one region: the
+        # clocks and the throughput of a sustained run beside the K-step figures.
+        n_long = max(1, int(math.ceil(1000.0 / (total_ms / args.steps))))
+        s1, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t_long0 = dt.datetime.now()
+        s1.record(stream)
+        for _ in range(n_long):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        t_long1 = dt.datetime.now()
+        long_ms = s1.elapsed_time(e1)
     barrier()
-    total_ms = start.elapsed_time(end)
     fwd_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
     bwd_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
+    main_ms = statistics.mean(e[3].elapsed_time(e[4]) for e in ev)
     if fa.status_check(dev) != abi.FA_OK:
         raise RuntimeError("device status after the timed region is not FA_OK")
 
@@ -269,9 +314,11 @@ def run_gpu(args, rank, world, local_rank):
     barrier()
     e2e_ms = s2.elapsed_time(e2)
 
-    total_ms, e2e_ms, fwd_ms, bwd_ms = ranks_max([total_ms, e2e_ms, fwd_ms, bwd_ms], world, dev)
-    return dict(total_ms=total_ms, fwd_ms=fwd_ms, bwd_ms=bwd_ms, e2e_ms=e2e_ms, h2d=h2d, d2h=d2h,
-                clocks=clocks.summary())
+    total_ms, e2e_ms, fwd_ms, bwd_ms, main_ms, long_ms = ranks_max(
+        [total_ms, e2e_ms, fwd_ms, bwd_ms, main_ms, long_ms], world, dev)
+    return dict(total_ms=total_ms, fwd_ms=fwd_ms, bwd_ms=bwd_ms, main_ms=main_ms, e2e_ms=e2e_ms, h2d=h2d,
+                d2h=d2h, long_steps=n_long, long_ms=long_ms, clocks=clocks.summary(t_start, t_end),
+                clocks_long=clocks.summary(t_long0, t_long1))
 
 
 # ------------------------------------------------------------------- sweep ----
@@ -514,25 +561,35 @@ def main():
     ms = r["total_ms"] / args.steps
     value = job_throughput(fwd_f + bwd_f, world, ms)
     peaks, src = load_peaks()
-    sustained = peaks.get("bf16_tflops_sustained") or peaks["bf16_tflops"]
+    burst = peaks["bf16_tflops"]
+    sustained = peaks.get("bf16_tflops_sustained") or burst
     bwd_tf = bwd_f / (r["bwd_ms"] * 1e-3) / 1e12
     fwd_tf = fwd_f / (r["fwd_ms"] * 1e-3) / 1e12
+    # the backward's FLOPs all run in its main kernel (the preprocess and the dQ conversion are
+    # elementwise passes): its roofline figure is those FLOPs over the main kernel's own time
+    main_tf = bwd_f / (r["main_ms"] * 1e-3) / 1e12
     e2e_ms = r["e2e_ms"] / args.steps
+    long_ms = r["long_ms"] / r["long_steps"]
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) x0.5, bf16)",
         "config": config_dict(),
-        "fwd": {"ms": r["fwd_ms"], "tflops": fwd_tf, "frac_of_sustained_peak": fwd_tf / sustained,
-                "frac_of_burst_peak": fwd_tf / peaks["bf16_tflops"]},
-        "bwd": {"ms": r["bwd_ms"], "tflops": bwd_tf, "frac_of_sustained_peak": bwd_tf / sustained,
-                "frac_of_burst_peak": bwd_tf / peaks["bf16_tflops"]},
-        "roofline": {"bound": "tensor", "kernel": "fa_bwd call (main kernel + prep + dq convert)",
-                     "achieved": bwd_tf, "peak": sustained, "unit": "TFLOP/s",
-                     "frac": bwd_tf / sustained, "peak_source": f"{src} bf16 sustained",
+        "fwd": {"ms": r["fwd_ms"], "tflops": fwd_tf, "frac_of_burst_peak": fwd_tf / burst,
+                "frac_of_sustained_peak": fwd_tf / sustained},
+        "bwd": {"ms": r["bwd_ms"], "tflops": bwd_tf, "frac_of_burst_peak": bwd_tf / burst,
+                "frac_of_sustained_peak": bwd_tf / sustained,
+                "main_kernel_ms": r["main_ms"], "main_kernel_share": r["main_ms"] / r["bwd_ms"]},
+        "roofline": {"bound": "tensor", "kernel": "fa_bwd_main_kernel<128, 2, causal>",
+                     "achieved": main_tf, "peak": burst, "unit": "TFLOP/s", "frac": main_tf / burst,
+                     "peak_source": f"{src} bf16 burst (of measured)" if src == "measured" else f"{src} bf16 burst",
+                     "frac_of_sustained": main_tf / sustained,
+                     "flops_per_launch": bwd_f, "ms_per_launch": r["main_ms"],
                      "traffic": kernel_traffic("fa_bwd.cu")},
         "e2e": {"value": world * (fwd_f + bwd_f) / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOPS",
                 "ms_per_step": e2e_ms, "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
+        "sustained": {"steps": r["long_steps"], "ms_per_step": long_ms,
+                      "value": job_throughput(fwd_f + bwd_f, world, long_ms), "clocks": r["clocks_long"]},
         "gpu_launches": 4 * args.steps,
         "clocks": r["clocks"],
     }

@@ -61,6 +61,7 @@ SIGNATURES = {
     "fa_status_check": (_c_int, [_c_void_p]),
     "fa_status_string": (ctypes.c_char_p, [_c_int]),
     "fa_set_wait_limit_ns": (ctypes.c_uint64, [ctypes.c_uint64]),
+    "fa_profile_next_bwd_main": (_c_int, [_c_void_p, _c_void_p]),
     "fa_test_withhold_kv_tile": (_c_int, [_c_int]),
 }
 
@@ -169,6 +170,10 @@ def fa_status_check(stream) -> int:
 
 def fa_set_wait_limit_ns(ns: int) -> int:
     return load().fa_set_wait_limit_ns(ns)
+
+
+def fa_profile_next_bwd_main(start_event, stop_event) -> int:
+    return load().fa_profile_next_bwd_main(start_event, stop_event)
 
 
 def fa_test_withhold_kv_tile(tile: int) -> int:

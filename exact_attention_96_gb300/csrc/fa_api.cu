@@ -25,6 +25,8 @@ int* g_err_ptr[kMaxDevices] = {};
 int g_cc_ok[kMaxDevices] = {};  // 0 unknown, 1 sm_103, -1 other
 std::atomic<uint64_t> g_wait_limit_ns{2000000000ull};
 std::atomic<int> g_withhold_k_tile{-1};  // one-shot test hook for the next fa_fwd launch
+// one-shot profiling request of this host thread: events around the next backward main kernel
+thread_local cudaEvent_t g_tl_main_events[2] = {nullptr, nullptr};
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
 fa_status cuda_fail(cudaError_t) { return FA_ERR_CUDA; }
@@ -236,12 +238,17 @@ fa_status bwd_impl(const void* q, const void* k, const void* v, const void* o, c
   a.wait_limit_ns = g_wait_limit_ns.load();
   a.err_word = err;
   a.dropout = dp ? *dp : fa::DropoutParams{0u, 1.f, 0u, 0u};
+  const cudaEvent_t events[2] = {g_tl_main_events[0], g_tl_main_events[1]};
+  g_tl_main_events[0] = g_tl_main_events[1] = nullptr;
   const cudaError_t e = fa::launch_bwd_all(maps, m_lse2, m_dvec, m_dk, m_dv, a, causal != 0, w.Np,
-                                           reinterpret_cast<cudaStream_t>(stream), dp != nullptr);
+                                           reinterpret_cast<cudaStream_t>(stream), dp != nullptr,
+                                           events[0] != nullptr ? events : nullptr);
   return e == cudaSuccess ? FA_OK : cuda_fail(e);
 }
 
 }  // namespace
+
+fa_status fa::check_problem_sizes(int B, int H, int N, int d) { return check_sizes(B, H, N, d); }
 
 extern "C" {
 
@@ -255,6 +262,13 @@ const char* fa_status_string(fa_status s) {
     case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT";
   }
   return "FA_ERR_UNKNOWN";
+}
+
+fa_status fa_profile_next_bwd_main(void* start_event, void* stop_event) {
+  if ((start_event == nullptr) != (stop_event == nullptr)) return FA_ERR_INVALID_ARG;
+  g_tl_main_events[0] = static_cast<cudaEvent_t>(start_event);
+  g_tl_main_events[1] = static_cast<cudaEvent_t>(stop_event);
+  return FA_OK;
 }
 
 int fa_test_withhold_kv_tile(int tile) { return g_withhold_k_tile.exchange(tile < 0 ? -1 : tile); }

@@ -680,29 +680,36 @@ cudaError_t launch_prep_and_convert(const BwdArgs& a, int Np, int n_q_tiles, cud
 // (tile order for d <= 128, row-major for d = 256).
 cudaError_t launch_bwd_all(const BwdMaps& m, const CUtensorMap& lse2, const CUtensorMap& dmap,
                            const CUtensorMap& dk, const CUtensorMap& dv, const BwdArgs& a, bool causal,
-                           int Np, cudaStream_t s, bool dropout) {
+                           int Np, cudaStream_t s, bool dropout, const cudaEvent_t* main_events) {
   const int n_q_tiles = (a.N + kTile - 1) / kTile;
+  if (a.d != 64 && a.d != 128 && a.d != 256) return cudaErrorInvalidValue;
   cudaError_t e;
   switch (a.d) {
+    case 64: e = launch_prep_and_convert<64>(a, Np, n_q_tiles, s, true); break;
+    case 128: e = launch_prep_and_convert<128>(a, Np, n_q_tiles, s, true); break;
+    default: e = launch_prep_and_convert<256>(a, Np, n_q_tiles, s, true); break;
+  }
+  if (e != cudaSuccess) return e;
+  if (main_events != nullptr && (e = cudaEventRecord(main_events[0], s)) != cudaSuccess) return e;
+  switch (a.d) {
     case 64:
-      if ((e = launch_prep_and_convert<64>(a, Np, n_q_tiles, s, true)) != cudaSuccess) return e;
       e = causal ? launch_main<64, 3, true>(m, lse2, dmap, dk, dv, a, s, dropout)
                  : launch_main<64, 3, false>(m, lse2, dmap, dk, dv, a, s, dropout);
-      if (e != cudaSuccess) return e;
-      return launch_prep_and_convert<64>(a, Np, n_q_tiles, s, false);
+      break;
     case 128:
-      if ((e = launch_prep_and_convert<128>(a, Np, n_q_tiles, s, true)) != cudaSuccess) return e;
       e = causal ? launch_main<128, 2, true>(m, lse2, dmap, dk, dv, a, s, dropout)
                  : launch_main<128, 2, false>(m, lse2, dmap, dk, dv, a, s, dropout);
-      if (e != cudaSuccess) return e;
-      return launch_prep_and_convert<128>(a, Np, n_q_tiles, s, false);
-    case 256:
-      if ((e = launch_prep_and_convert<256>(a, Np, n_q_tiles, s, true)) != cudaSuccess) return e;
-      e = launch_bwd_main_d256(m.q64, m.k, m.v, m.dout64, m.lse2_64, m.dvec_64, dk, dv, a, causal, s, dropout);
-      if (e != cudaSuccess) return e;
-      return launch_prep_and_convert<256>(a, Np, n_q_tiles, s, false);
+      break;
     default:
-      return cudaErrorInvalidValue;
+      e = launch_bwd_main_d256(m.q64, m.k, m.v, m.dout64, m.lse2_64, m.dvec_64, dk, dv, a, causal, s, dropout);
+      break;
+  }
+  if (e != cudaSuccess) return e;
+  if (main_events != nullptr && (e = cudaEventRecord(main_events[1], s)) != cudaSuccess) return e;
+  switch (a.d) {
+    case 64: return launch_prep_and_convert<64>(a, Np, n_q_tiles, s, false);
+    case 128: return launch_prep_and_convert<128>(a, Np, n_q_tiles, s, false);
+    default: return launch_prep_and_convert<256>(a, Np, n_q_tiles, s, false);
   }
 }
 

@@ -7,9 +7,14 @@
 #include <cstddef>
 #include <cstdint>
 
+#include "../../include/fa.h"
 #include "philox.cuh"
 
 namespace fa {
+
+// The size checks every entry point applies (B, H, N >= 1; d in {64, 128, 256}; B*H and N
+// within the ABI's limits): FA_OK, FA_ERR_INVALID_ARG or FA_ERR_UNSUPPORTED (fa_api.cu).
+fa_status check_problem_sizes(int B, int H, int N, int d);
 
 #ifdef __CUDACC__
 // Dispatch order of causal launches.  A causal CTA's work depends on its tile: with rank
@@ -117,9 +122,11 @@ cudaError_t launch_bwd_main_d256(const CUtensorMap& q64, const CUtensorMap& k, c
 // Backward: prep, main and dQ-convert launches.  `lse2` and `dvec` describe the fp32
 // [B*H, Np] rows of the workspace (box 128 x 1 x 1); `dk`, `dv` the bf16 outputs.
 // Np = N rounded up to a multiple of 4.
-// With `dropout` the main kernel applies the mask of a.dropout.
+// With `dropout` the main kernel applies the mask of a.dropout.  `main_events` (optional, two
+// events) are recorded on `s` just before and just after the main kernel's launch.
 cudaError_t launch_bwd_all(const BwdMaps& m, const CUtensorMap& lse2, const CUtensorMap& dvec,
                            const CUtensorMap& dk, const CUtensorMap& dv, const BwdArgs& a,
-                           bool causal, int Np, cudaStream_t s, bool dropout = false);
+                           bool causal, int Np, cudaStream_t s, bool dropout = false,
+                           const cudaEvent_t* main_events = nullptr);
 
 }  // namespace fa

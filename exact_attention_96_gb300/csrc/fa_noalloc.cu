@@ -2,12 +2,11 @@
 // device memory.
 //
 // fa_bwd needs a caller-provided workspace (D, LSE*log2e and the fp32 dQ accumulator).
-// Some callers cannot obtain one: code running while a stream is being captured into a
-// CUDA graph (cudaMalloc is not allowed there), code that must not trigger the implicit
-// device synchronisation a cudaMalloc/cudaFree can cause, and embedders whose device
-// memory is wholly owned by another allocator they cannot call from here.  For them this
-// entry point uses a fixed scratch array that lives in the library's static device memory
-// instead: it allocates nothing and frees nothing.
+// Some callers cannot obtain one: embedders whose device memory is wholly owned by another
+// allocator they cannot call from here, and code that must not trigger the implicit device
+// synchronisation a cudaMalloc/cudaFree can cause.  For them this entry point uses a fixed
+// scratch array that lives in the library's static device memory instead: it allocates
+// nothing and frees nothing.
 //
 // The array is FA_NOALLOC_SCRATCH_BYTES (64 MiB) on every device that loads the library
 // and stays allocated until the process exits.  Host code cannot use the array's name as a
@@ -23,6 +22,7 @@
 #include <mutex>
 
 #include "../../include/fa.h"
+#include "fa_internal.h"
 
 namespace {
 
@@ -38,9 +38,9 @@ extern "C" fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v,
                                     const void* dout, const float* lse, void* dq, void* dk, void* dv,
                                     int B, int H, int N, int d, float scale, int causal,
                                     fa_stream_t stream) {
-  const size_t need = fa_bwd_workspace_bytes(B, H, N, d);
-  if (need == 0) return (B < 1 || H < 1 || N < 1) ? FA_ERR_INVALID_ARG : FA_ERR_UNSUPPORTED;
-  if (need > FA_NOALLOC_SCRATCH_BYTES) return FA_ERR_UNSUPPORTED;
+  const fa_status sizes = fa::check_problem_sizes(B, H, N, d);
+  if (sizes != FA_OK) return sizes;
+  if (fa_bwd_workspace_bytes(B, H, N, d) > FA_NOALLOC_SCRATCH_BYTES) return FA_ERR_UNSUPPORTED;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
   if (dev < 0 || dev >= kMaxDevices) return FA_ERR_UNSUPPORTED;

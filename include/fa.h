@@ -172,11 +172,11 @@ fa_status fa_bwd_dropout(const void* q, const void* k, const void* v, const void
 
 /*
  * fa_bwd_noalloc -- the backward pass of fa_bwd for callers that cannot allocate device
- * memory (the pages have no counterpart: this is a deployment convenience).  Examples of
- * such callers: code running while a stream is being captured into a CUDA graph, where
- * cudaMalloc is not allowed; latency-critical code that must not hit the implicit device
- * synchronisation of cudaMalloc / cudaFree; embedders whose device memory belongs to an
- * allocator they cannot reach from here.
+ * memory (the pages have no counterpart: this is a deployment convenience).  Such callers
+ * include embedders whose device memory belongs wholly to an allocator they cannot reach from
+ * here (a host application or framework that hands out no buffers to plug-ins), and
+ * latency-critical code that must not hit the implicit device synchronisation of cudaMalloc /
+ * cudaFree in the middle of its work.
  *
  * Arguments and results are those of fa_bwd without the workspace: the workspace is a
  * file-scope static device array of FA_NOALLOC_SCRATCH_BYTES, held by every device that
@@ -238,6 +238,18 @@ const char* fa_status_string(fa_status s);
  * Applies to launches made after the call, on every device.  Returns the previous value.
  */
 uint64_t fa_set_wait_limit_ns(uint64_t ns);
+
+/*
+ * Profiling hook (not needed in normal use).  The next backward call made by the calling
+ * host thread (fa_bwd, fa_bwd_dropout or fa_bwd_noalloc) records `start_event` on its stream
+ * just before it launches its main kernel (the pass over key tiles that recomputes S and P,
+ * "FlashAttention 与显存" §09) and `stop_event` just after, so that the elapsed time between
+ * the two events is that kernel's alone, without the D preprocess and the dQ conversion.
+ * Both are cudaEvent_t handles created by the caller (with timing enabled) on the current
+ * device.  One-shot: the call consumes the request; two null pointers cancel it.
+ * Returns FA_OK, or FA_ERR_INVALID_ARG when exactly one of the two is null.
+ */
+fa_status fa_profile_next_bwd_main(void* start_event, void* stop_event);
 
 /*
  * Test hook for the failure path (not needed in normal use).  The next fa_fwd launch, on any

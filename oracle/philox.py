@@ -18,9 +18,11 @@ kept when that half is >= t = min(round(p * 2^16), 2^16 - 1), i.e. with probabil
 (2^16 - t) / 2^16, and kept elements are scaled by the inverse of that probability, so the
 mask's expectation is exactly 1 (p is quantised to multiples of 2^-16).
 
-Parity unpinned: the identity of ``philox4x32_10`` with the published generator (no
-known-answer vectors are reproduced here).  What the method needs from the mask -- keep rate,
-uniform draws, dependence on every coordinate, unbiasedness -- is pinned by the tests.
+Pinned against an independent implementation of the same generator: cuRAND's host-side
+PHILOX4_32_10 generator, whose output stream is Philox4x32-10 of a known counter sequence
+(tests/test_oracle_dropout.py compares them bit for bit, over the key, the three counter words
+the mask fills and counters up to 2^62).  What the method needs from the mask -- keep rate,
+uniform draws, dependence on every coordinate, unbiasedness -- is pinned by the same tests.
 """
 
 from __future__ import annotations

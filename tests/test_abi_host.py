@@ -116,6 +116,12 @@ def test_withhold_hook_is_one_shot_request(lib):
     assert abi.fa_test_withhold_kv_tile(-1) == -1
 
 
+def test_profile_hook_wants_both_events_or_neither(lib):
+    assert abi.fa_profile_next_bwd_main(FAKE, None) == abi.FA_ERR_INVALID_ARG
+    assert abi.fa_profile_next_bwd_main(None, FAKE) == abi.FA_ERR_INVALID_ARG
+    assert abi.fa_profile_next_bwd_main(None, None) == abi.FA_OK  # cancels
+
+
 def test_split_plan(lib):
     # every range non-empty; auto picks about two CTAs per SM for decode shapes
     n = abi.fa_fwd_splitkv_num_splits

@@ -1,10 +1,15 @@
 """Pins of the oracle's dropout (mask generator and dropout arithmetic).
 
-The generator is checked by its statistics and its dependence on every counter field; the
-arithmetic by reduction to the plain path at p = 0, by unbiasedness over seeds, by central
-finite differences at a fixed mask, and by torch (softmax and autograd) applied to P * Z."""
+The generator is checked against an independent implementation of the same published
+generator, cuRAND's host-side PHILOX4_32_10 generator (run on the CPU, no GPU needed), and by
+its statistics and its dependence on every counter field; the arithmetic by reduction to the
+plain path at p = 0, by unbiasedness over seeds, by central finite differences at a fixed mask,
+and by torch (softmax and autograd) applied to P * Z."""
 
+import ctypes
+import ctypes.util
 import math
+import os
 
 import numpy as np
 import pytest
@@ -17,6 +22,87 @@ from oracle import philox
 
 def rnd(shape, seed):
     return np.random.default_rng(seed).standard_normal(shape)
+
+
+# ----------------------------------------------------------------------------------------
+# Philox4x32-10 against cuRAND's host generator.
+#
+# cuRAND's host generator of type CURAND_RNG_PSEUDO_PHILOX4_32_10 (created with
+# curandCreateGeneratorHost, so it runs on the host) is another implementation of the
+# generator of Salmon et al. (SC 2011).  With seed s its key is (s mod 2^32, s >> 32).  Its
+# output stream, observed over 2^24 values and at offsets up to 2^64, is made of blocks of four
+# 32-bit words: with generator offset 4m, block b = m + n (the n-th group of four outputs) is
+# Philox4x32-10 of the counter (floor(b / 2^16) mod 2^32, floor(b / 2^48), b mod 2^16, 0).  So
+# the comparison covers the key, both multipliers, the Weyl bumps, the round count, the output
+# word order and the counter words c0, c1 and c2 -- the three the dropout mask fills (key
+# tile, query row, head); c3 is always 0 there.
+
+_CURAND_PHILOX = 161  # curandRngType_t CURAND_RNG_PSEUDO_PHILOX4_32_10
+
+
+def _curand():
+    names = [os.path.join(os.environ.get("CUDA_HOME", "/usr/local/cuda"), "lib64", "libcurand.so"),
+             ctypes.util.find_library("curand"), "libcurand.so.10"]
+    for name in names:
+        if not name:
+            continue
+        try:
+            return ctypes.CDLL(name)
+        except OSError:
+            continue
+    pytest.skip("cuRAND (libcurand.so) not found")
+
+
+def _curand_philox_blocks(lib, seed: int, offset_blocks: int, n_blocks: int) -> np.ndarray:
+    gen = ctypes.c_void_p()
+    assert lib.curandCreateGeneratorHost(ctypes.byref(gen), _CURAND_PHILOX) == 0
+    try:
+        assert lib.curandSetPseudoRandomGeneratorSeed(gen, ctypes.c_ulonglong(seed)) == 0
+        assert lib.curandSetGeneratorOffset(gen, ctypes.c_ulonglong(4 * offset_blocks)) == 0
+        out = np.zeros(4 * n_blocks, np.uint32)
+        assert lib.curandGenerate(gen, out.ctypes.data_as(ctypes.c_void_p), ctypes.c_size_t(out.size)) == 0
+    finally:
+        lib.curandDestroyGenerator(gen)
+    return out.reshape(-1, 4)
+
+
+def _oracle_blocks(philox4x32_10, seed: int, offset_blocks: int, n_blocks: int) -> np.ndarray:
+    b = [offset_blocks + n for n in range(n_blocks)]  # python ints: offsets reach 2^62
+    c0 = np.array([(x >> 16) & 0xFFFFFFFF for x in b], np.uint64)
+    c1 = np.array([x >> 48 for x in b], np.uint64)
+    c2 = np.array([x & 0xFFFF for x in b], np.uint64)
+    words = philox4x32_10(c0, c1, c2, np.zeros_like(c0), seed & 0xFFFFFFFF, seed >> 32)
+    return np.stack(words, 1)
+
+
+PHILOX_CASES = [  # (seed, first block, blocks): the first spans the c2 -> c0 carry at 2^16
+    (0x0123456789ABCDEF, 0, 1 << 17),
+    (0, 12345, 4096),
+    (0xFFFFFFFFFFFFFFFF, (1 << 32) + 77, 4096),
+    (0xDEADBEEF12345678, (1 << 48) + (1 << 20) + 5, 4096),
+    (7, (1 << 62) - 12345, 4096),
+]
+
+
+@pytest.mark.parametrize("seed,first,n", PHILOX_CASES)
+def test_philox_matches_curand_host_generator(seed, first, n):
+    lib = _curand()
+    want = _curand_philox_blocks(lib, seed, first, n)
+    got = _oracle_blocks(philox.philox4x32_10, seed, first, n)
+    assert np.array_equal(got, want)
+
+
+@pytest.mark.parametrize("mistake", [dict(M0=philox.M1, M1=philox.M0), dict(M0=philox.M0 + np.uint64(2)),
+                                     dict(W0=philox.W1, W1=philox.W0), dict(W1=np.uint32(0))])
+def test_philox_comparison_catches_planted_mistakes(mistake, monkeypatch):
+    """A mistake planted in the oracle's constants (swapped or altered multipliers, swapped or
+    missing key bumps) makes the comparison with cuRAND fail."""
+    lib = _curand()
+    seed, first, n = PHILOX_CASES[3]
+    want = _curand_philox_blocks(lib, seed, first, n)
+    for name, value in mistake.items():
+        monkeypatch.setattr(philox, name, value)
+    assert not np.array_equal(_oracle_blocks(philox.philox4x32_10, seed, first, n), want)
 
 
 @pytest.mark.parametrize("p", [0.1, 0.5, 0.9])
