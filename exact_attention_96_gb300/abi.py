@@ -44,6 +44,11 @@ SIGNATURES = {
                         _c_void_p, _c_void_p, _c_void_p,
                         _c_int, _c_int, _c_int, _c_int, _c_float, _c_int,
                         _c_void_p, _c_size_t, _c_void_p]),
+    "fa_bwd_accumulate": (_c_int, [_c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_void_p,
+                                   _c_void_p, _c_void_p, _c_void_p,
+                                   _c_int, _c_int, _c_int, _c_int, _c_float, _c_int,
+                                   _c_void_p, _c_size_t, _c_void_p]),
+    "fa_convert_f32_to_bf16": (_c_int, [_c_void_p, _c_void_p, ctypes.c_longlong, _c_void_p]),
     "fa_fwd_dropout": (_c_int, [_c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_void_p,
                                 _c_int, _c_int, _c_int, _c_int, _c_float, _c_int,
                                 ctypes.c_double, ctypes.c_ulonglong, _c_void_p]),
@@ -137,6 +142,16 @@ def fa_bwd_workspace_bytes(B, H, N, d) -> int:
 def fa_bwd(q, k, v, o, do, lse, dq, dk, dv, B, H, N, d, scale, causal, ws, ws_bytes, stream) -> int:
     return load().fa_bwd(q, k, v, o, do, lse, dq, dk, dv, B, H, N, d, scale, int(causal),
                          ws, ws_bytes, stream)
+
+
+def fa_bwd_accumulate(q, k, v, o, do, lse, dq_acc, dk_acc, dv_acc, B, H, N, d, scale, causal, ws, ws_bytes,
+                      stream) -> int:
+    return load().fa_bwd_accumulate(q, k, v, o, do, lse, dq_acc, dk_acc, dv_acc, B, H, N, d, scale, int(causal),
+                                    ws, ws_bytes, stream)
+
+
+def fa_convert_f32_to_bf16(src, dst, n, stream) -> int:
+    return load().fa_convert_f32_to_bf16(src, dst, n, stream)
 
 
 def fa_fwd_dropout(q, k, v, o, lse, B, H, N, d, scale, causal, dropout_p, seed, stream) -> int:

@@ -184,11 +184,19 @@ fa_status fwd_impl(const void* q, const void* k, const void* v, void* o, float* 
   return e == cudaSuccess ? FA_OK : cuda_fail(e);
 }
 
-// Backward; `dp` null: no dropout (with dropout d <= 128).
+// Backward; `dp` null: no dropout.  `accum` (three fp32 pointers dQ, dK, dV) selects the
+// accumulate mode, where dq, dk, dv are not used.
 fa_status bwd_impl(const void* q, const void* k, const void* v, const void* o, const void* dout,
                    const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d, float scale,
                    int causal, const fa::DropoutParams* dp, void* workspace, size_t workspace_bytes,
-                   fa_stream_t stream) {
+                   fa_stream_t stream, float* const* accum = nullptr) {
+  if (accum != nullptr) {
+    if (!accum[0] || !accum[1] || !accum[2]) return FA_ERR_INVALID_ARG;
+    if (!aligned16(accum[0]) || !aligned16(accum[1]) || !aligned16(accum[2])) return FA_ERR_MISALIGNED;
+    dq = accum[0];  // stand-ins: the bf16 outputs are neither encoded for stores nor written
+    dk = accum[1];
+    dv = accum[2];
+  }
   if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv || !workspace) return FA_ERR_INVALID_ARG;
   fa_status st = check_sizes(B, H, N, d);
   if (st != FA_OK) return st;
@@ -238,6 +246,9 @@ fa_status bwd_impl(const void* q, const void* k, const void* v, const void* o, c
   a.wait_limit_ns = g_wait_limit_ns.load();
   a.err_word = err;
   a.dropout = dp ? *dp : fa::DropoutParams{0u, 1.f, 0u, 0u};
+  a.dq_accum = accum ? accum[0] : nullptr;
+  a.dk_accum = accum ? accum[1] : nullptr;
+  a.dv_accum = accum ? accum[2] : nullptr;
   const cudaEvent_t events[2] = {g_tl_main_events[0], g_tl_main_events[1]};
   g_tl_main_events[0] = g_tl_main_events[1] = nullptr;
   const cudaError_t e = fa::launch_bwd_all(maps, m_lse2, m_dvec, m_dk, m_dv, a, causal != 0, w.Np,
@@ -438,6 +449,27 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
                  int causal, void* workspace, size_t workspace_bytes, fa_stream_t stream) {
   return bwd_impl(q, k, v, o, dout, lse, dq, dk, dv, B, H, N, d, scale, causal, nullptr, workspace,
                   workspace_bytes, stream);
+}
+
+fa_status fa_bwd_accumulate(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                            const float* lse, float* dq_acc, float* dk_acc, float* dv_acc, int B, int H, int N,
+                            int d, float scale, int causal, void* workspace, size_t workspace_bytes,
+                            fa_stream_t stream) {
+  float* const accum[3] = {dq_acc, dk_acc, dv_acc};
+  return bwd_impl(q, k, v, o, dout, lse, nullptr, nullptr, nullptr, B, H, N, d, scale, causal, nullptr,
+                  workspace, workspace_bytes, stream, accum);
+}
+
+fa_status fa_convert_f32_to_bf16(const float* src, void* dst, long long n, fa_stream_t stream) {
+  if (!src || !dst || n < 1) return FA_ERR_INVALID_ARG;
+  if (!aligned16(src) || !aligned16(dst)) return FA_ERR_MISALIGNED;
+  int dev = 0;
+  int* err = nullptr;
+  const fa_status st = device_setup(&dev, &err);
+  if (st != FA_OK) return st;
+  const cudaError_t e = fa::launch_f32_to_bf16(src, static_cast<uint16_t*>(dst), n,
+                                               reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : cuda_fail(e);
 }
 
 fa_status fa_bwd_dropout(const void* q, const void* k, const void* v, const void* o, const void* dout,

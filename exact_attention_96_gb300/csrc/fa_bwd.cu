@@ -112,10 +112,37 @@ fa_bwd_prep_kernel(const uint16_t* __restrict__ o, const uint16_t* __restrict__ 
 
 // ------------------------------------------------------------ dq convert ----
 
+// dst[0..8) += scale * (a, b)
+__device__ __forceinline__ void add_scaled8(float* dst, float4 a, float4 b, float scale) {
+  float4* d4 = reinterpret_cast<float4*>(dst);
+  float4 x = d4[0], y = d4[1];
+  x.x += a.x * scale; x.y += a.y * scale; x.z += a.z * scale; x.w += a.w * scale;
+  y.x += b.x * scale; y.y += b.y * scale; y.z += b.z * scale; y.w += b.w * scale;
+  d4[0] = x;
+  d4[1] = y;
+}
+
+// fp32 -> bf16, eight elements per thread (the tail element by element).
+__global__ void __launch_bounds__(256)
+fa_f32_to_bf16_kernel(const float* __restrict__ src, uint16_t* __restrict__ dst, long long n) {
+  const long long i0 = ((long long)blockIdx.x * 256 + threadIdx.x) * 8;
+  if (i0 + 8 <= n) {
+    const float4 a = *reinterpret_cast<const float4*>(src + i0);
+    const float4 b = *reinterpret_cast<const float4*>(src + i0 + 4);
+    *reinterpret_cast<uint4*>(dst + i0) =
+        make_uint4(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w), pack_bf16x2(b.x, b.y), pack_bf16x2(b.z, b.w));
+  } else {
+    for (long long i = i0; i < n; ++i) dst[i] = uint16_t(pack_bf16x2(src[i], 0.f) & 0xFFFFu);
+  }
+}
+
+// With `dq_out` set (accumulate mode) scale * accumulator is added into that fp32 row-major
+// buffer instead of being written as bf16: each element has one owner thread, and calls on one
+// stream are ordered, so a plain read-add-write is enough.
 template <int D>
 __global__ void __launch_bounds__(256)
-fa_bwd_dq_kernel(const float* __restrict__ dq_acc, uint16_t* __restrict__ dq, int N, int n_q_tiles,
-                 int BH, float scale) {
+fa_bwd_dq_kernel(const float* __restrict__ dq_acc, uint16_t* __restrict__ dq, float* __restrict__ dq_out,
+                 int N, int n_q_tiles, int BH, float scale) {
   constexpr int kK = D / 8;
   const long long gid = (long long)blockIdx.x * 256 + threadIdx.x;
   if constexpr (D == 256) {  // row-major accumulator: thread -> (padded row, 8 columns k)
@@ -127,6 +154,10 @@ fa_bwd_dq_kernel(const float* __restrict__ dq_acc, uint16_t* __restrict__ dq, in
     if (i >= N) return;
     const float4* src = reinterpret_cast<const float4*>(dq_acc + (size_t)prow * D) + 2 * k;
     const float4 a = src[0], b = src[1];
+    if (dq_out != nullptr) {
+      add_scaled8(dq_out + ((size_t)bh * N + i) * D + k * 8, a, b, scale);
+      return;
+    }
     uint4 w;
     w.x = pack_bf16x2(a.x * scale, a.y * scale);
     w.y = pack_bf16x2(a.z * scale, a.w * scale);
@@ -148,6 +179,10 @@ fa_bwd_dq_kernel(const float* __restrict__ dq_acc, uint16_t* __restrict__ dq, in
   const float4* src = reinterpret_cast<const float4*>(dq_acc + (size_t)tile * 128 * D);
   const float4 a = src[(2 * k) * 128 + t];
   const float4 b = src[(2 * k + 1) * 128 + t];
+  if (dq_out != nullptr) {
+    add_scaled8(dq_out + ((size_t)bh * N + i) * D + k * 8, a, b, scale);
+    return;
+  }
   uint4 w;
   w.x = pack_bf16x2(a.x * scale, a.y * scale);
   w.y = pack_bf16x2(a.z * scale, a.w * scale);
@@ -575,7 +610,24 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
     const uint32_t col = half == 0 ? L::kColDV : L::kColDK;
     const float mul = half == 0 ? (DROPOUT ? args.dropout.scale : 1.f) : args.scale;
     uint8_t* stage = smem + (half == 0 ? L::kQOff : L::kdOOff);
-    if (fin) {
+    const bool accum = args.dk_accum != nullptr;
+    if (fin && accum) {
+      // accumulate mode: add the fp32 rows into the caller's buffers (vector atomics)
+      tc_fence_after_sync();
+      float4* dst = reinterpret_cast<float4*>((half == 0 ? args.dv_accum : args.dk_accum) +
+                                              ((size_t)bh * N + key) * D);
+#pragma unroll 1
+      for (int c = 0; c < D; c += 32) {
+        uint32_t r[32];
+        tmem_ld32(tmem + lane_off + col + c, r);
+        if (key < N) {
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            atomicAdd(dst + c / 4 + e, make_float4(__uint_as_float(r[4 * e]) * mul, __uint_as_float(r[4 * e + 1]) * mul,
+                                                   __uint_as_float(r[4 * e + 2]) * mul, __uint_as_float(r[4 * e + 3]) * mul));
+        }
+      }
+    } else if (fin) {
       tc_fence_after_sync();
 #pragma unroll 1
       for (int c = 0; c < D; c += 32) {
@@ -597,7 +649,7 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
       fence_proxy_async_smem();
     }
     mbar_arrive(bar(L::kBarEpi + half));
-    if (t == 0 && fin && mbar_wait(bar(L::kBarEpi + half), 0, wc) && *abort_flag == 0) {
+    if (t == 0 && fin && !accum && mbar_wait(bar(L::kBarEpi + half), 0, wc) && *abort_flag == 0) {
       const CUtensorMap* map = half == 0 ? &tmdV : &tmdK;
       const uint32_t src = half == 0 ? sQ(0) : sdO(0);
       for (int s = 0; s < L::kSlabs; ++s) tma_store_3d(map, src + s * (kTile * 128), s * 64, k0, bh);
@@ -669,12 +721,18 @@ cudaError_t launch_prep_and_convert(const BwdArgs& a, int Np, int n_q_tiles, cud
   } else {
     const long long total = (long long)a.BH * n_q_tiles * 128 * (D / 8);
     const unsigned grid = unsigned((total + 255) / 256);
-    fa_bwd_dq_kernel<D><<<grid, 256, 0, s>>>(a.dq_acc, a.dq, a.N, n_q_tiles, a.BH, a.scale);
+    fa_bwd_dq_kernel<D><<<grid, 256, 0, s>>>(a.dq_acc, a.dq, a.dq_accum, a.N, n_q_tiles, a.BH, a.scale);
   }
   return cudaGetLastError();
 }
 
 }  // namespace
+
+cudaError_t launch_f32_to_bf16(const float* src, uint16_t* dst, long long n, cudaStream_t s) {
+  const long long threads = (n + 7) / 8;
+  fa_f32_to_bf16_kernel<<<unsigned((threads + 255) / 256), 256, 0, s>>>(src, dst, n);
+  return cudaGetLastError();
+}
 
 // Workspace: [D: BH x Np][LSE2: BH x Np][dQ accumulator: BH x n_q_tiles x 128 x d], fp32
 // (tile order for d <= 128, row-major for d = 256).

@@ -350,7 +350,24 @@ fa_bwd_d256_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
     const uint32_t col = half == 0 ? L::kColDV : L::kColDK;
     const float mul = half == 0 ? (DROPOUT ? args.dropout.scale : 1.f) : args.scale;
     uint8_t* stage = smem + (half == 0 ? L::kQOff : L::kdOOff);   // 2 slabs of [128 x 128 B]
-    if (fin) {
+    const bool accum = args.dk_accum != nullptr;
+    if (fin && accum) {
+      // accumulate mode: add the fp32 slice rows into the caller's buffers (vector atomics)
+      tc_fence_after_sync();
+      float4* dst = reinterpret_cast<float4*>((half == 0 ? args.dv_accum : args.dk_accum) +
+                                              ((size_t)bh * N + key) * 256 + kDH * z);
+#pragma unroll 1
+      for (int c = 0; c < kDH; c += 32) {
+        uint32_t r[32];
+        tmem_ld32(tmem + lane_off + col + c, r);
+        if (key < N) {
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            atomicAdd(dst + c / 4 + e, make_float4(__uint_as_float(r[4 * e]) * mul, __uint_as_float(r[4 * e + 1]) * mul,
+                                                   __uint_as_float(r[4 * e + 2]) * mul, __uint_as_float(r[4 * e + 3]) * mul));
+        }
+      }
+    } else if (fin) {
       tc_fence_after_sync();
 #pragma unroll 1
       for (int c = 0; c < kDH; c += 32) {
@@ -373,7 +390,7 @@ fa_bwd_d256_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
     }
     const uint32_t epi = bar(half == 0 ? L::kBarEpi0 : L::kBarEpi1);
     mbar_arrive(epi);
-    if (t == 0 && fin && mbar_wait(epi, 0, wc) && *abort_flag == 0) {
+    if (t == 0 && fin && !accum && mbar_wait(epi, 0, wc) && *abort_flag == 0) {
       const CUtensorMap* map = half == 0 ? &tmdV : &tmdK;
       const uint32_t src = half == 0 ? sQ : sdO;
       for (int s = 0; s < 2; ++s) tma_store_3d(map, src + s * (kKeys * 128), kDH * z + 64 * s, k0, bh);

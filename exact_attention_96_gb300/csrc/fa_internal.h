@@ -104,6 +104,12 @@ struct BwdArgs {
   uint64_t wait_limit_ns;
   int* err_word;
   DropoutParams dropout;  // threshold 0 with scale 1: no dropout
+  // Accumulate mode (all three set, or all null): the gradients are added in fp32 into these
+  // caller buffers ([B*H, N, d] row-major, dQ already multiplied by the scale) instead of
+  // being written as bf16 dq, dk, dv.
+  float* dq_accum;
+  float* dk_accum;
+  float* dv_accum;
 };
 
 struct BwdMaps {
@@ -128,5 +134,8 @@ cudaError_t launch_bwd_all(const BwdMaps& m, const CUtensorMap& lse2, const CUte
                            const CUtensorMap& dk, const CUtensorMap& dv, const BwdArgs& a,
                            bool causal, int Np, cudaStream_t s, bool dropout = false,
                            const cudaEvent_t* main_events = nullptr);
+
+// fp32 -> bf16 (round to nearest even), n elements, 16-byte aligned pointers.
+cudaError_t launch_f32_to_bf16(const float* src, uint16_t* dst, long long n, cudaStream_t s);
 
 }  // namespace fa

@@ -7,7 +7,8 @@ On a ring of `world` workers, at hop t worker r holds the key/value shard that s
 worker (r - t) mod world.  With a causal mask worker r needs only shards s <= r, the shard
 s == r with the causal mask of the diagonal block.  Here every worker runs in turn on the same
 GPU, so "passing a shard" is indexing; each hop calls fa_fwd_partial and each worker's hops are
-merged by fa_merge_partials.
+merged by fa_merge_partials.  The backward pass runs one fa_bwd_accumulate per (worker, shard)
+pair into fp32 per-shard accumulators and rounds the sums once (fa_convert_f32_to_bf16).
 """
 
 from __future__ import annotations
@@ -67,10 +68,12 @@ def ring_attention_backward(q, k, v, o, do, lse, world: int, causal: bool = Fals
                             scale: float | None = None):
     """dQ, dK, dV of ring attention.  With the global LSE (from the forward) every
     probability is fixed, so the contribution of query shard r and key/value shard s is
-    exactly the backward pass of that block pair (fa_bwd with O_r, dO_r and LSE_r; the
-    diagonal pair causal, later shards skipped).  Worker r accumulates dQ_r over the shards
-    it sees; dK_s, dV_s collect the contributions of every worker that saw shard s (on a
-    real ring they travel back with the shard).  The sums are fp32."""
+    exactly the backward pass of that block pair (O_r, dO_r and LSE_r of the whole problem;
+    the diagonal pair causal, later shards skipped).  Worker r accumulates dQ_r over the shards
+    it sees; dK_s, dV_s collect the contributions of every worker that saw shard s (on a real
+    ring they travel back with the shard).  fa_bwd_accumulate adds each block pair's
+    contribution in fp32 into per-shard accumulators, and fa_convert_f32_to_bf16 rounds each
+    sum once at the end."""
     from . import attention as fa  # local import: attention imports nothing from here
 
     B, H, N, d = q.shape
@@ -79,17 +82,22 @@ def ring_attention_backward(q, k, v, o, do, lse, world: int, causal: bool = Fals
     ns = N // world
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
     shard = lambda t, i: t[:, :, i * ns:(i + 1) * ns].contiguous()  # noqa: E731
-    dq = torch.zeros(q.shape, dtype=torch.float32, device=q.device)
-    dk = torch.zeros(k.shape, dtype=torch.float32, device=q.device)
-    dv = torch.zeros(v.shape, dtype=torch.float32, device=q.device)
+    # fp32 accumulators, shard-major: acc[g, s] is gradient g (dQ, dK, dV) of shard s
+    acc = torch.zeros((3, world, B, H, ns, d), dtype=torch.float32, device=q.device)
     ws = torch.empty(fa.workspace_bytes(B, H, ns, d), dtype=torch.uint8, device=q.device)
-    grads = tuple(torch.empty((B, H, ns, d), dtype=q.dtype, device=q.device) for _ in range(3))
+    stream = torch.cuda.current_stream(q.device).cuda_stream
+    k_sh = [shard(k, s) for s in range(world)]
+    v_sh = [shard(v, s) for s in range(world)]
     for r in range(world):
         q_r, o_r, do_r, lse_r = shard(q, r), shard(o, r), shard(do, r), shard(lse, r)
         for _, s, diag in ring_hops(r, world, causal):
-            g_q, g_k, g_v = fa.backward(q_r, shard(k, s), shard(v, s), o_r, do_r, lse_r,
-                                        causal=causal and diag, scale=scale, workspace=ws, grads=grads)
-            dq[:, :, r * ns:(r + 1) * ns] += g_q.float()
-            dk[:, :, s * ns:(s + 1) * ns] += g_k.float()
-            dv[:, :, s * ns:(s + 1) * ns] += g_v.float()
-    return dq.to(q.dtype), dk.to(k.dtype), dv.to(v.dtype)
+            abi.check("fa_bwd_accumulate", abi.fa_bwd_accumulate(
+                q_r.data_ptr(), k_sh[s].data_ptr(), v_sh[s].data_ptr(), o_r.data_ptr(), do_r.data_ptr(),
+                lse_r.data_ptr(), acc[0, r].data_ptr(), acc[1, s].data_ptr(), acc[2, s].data_ptr(),
+                B, H, ns, d, scale, causal and diag, ws.data_ptr(), ws.numel(), stream))
+    out = torch.empty(acc.shape, dtype=q.dtype, device=q.device)
+    abi.check("fa_convert_f32_to_bf16", abi.fa_convert_f32_to_bf16(acc.data_ptr(), out.data_ptr(),
+                                                                   acc.numel(), stream))
+    # shard-major [world, B, H, ns, d] -> [B, H, N, d] (a copy, no arithmetic)
+    dq, dk, dv = (out[g].permute(1, 2, 0, 3, 4).reshape(B, H, N, d) for g in range(3))
+    return dq, dk, dv

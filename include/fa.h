@@ -141,6 +141,36 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
                  void* workspace, size_t workspace_bytes, fa_stream_t stream);
 
 /*
+ * Backward pass of one block pair, accumulated in fp32 (ring attention, "Flash Attention
+ * 原理与实践" §5.2: a worker's queries meet every key/value shard in turn, so its dQ is the sum
+ * of one contribution per shard, and a shard's dK, dV the sum of one contribution per worker
+ * that held it).  With the LSE of the whole problem (the merged one of fa_merge_partials) every
+ * probability of the block pair is fixed, so its contribution is the backward pass of that
+ * block pair alone, as fa_bwd computes it with these arguments:
+ *   q, o, dout, lse: one query block (bf16 [B,H,N,d], fp32 [B,H,N]) with the O, dO and LSE of
+ *   the whole problem for its rows; k, v: one key/value block of the same length N;
+ *   causal != 0 for a diagonal block (key j hidden from query i when j > i, local indices).
+ * Instead of writing bf16 gradients it ADDS, in fp32, dQ into dq_acc, dK into dk_acc and dV
+ * into dv_acc (each fp32 [B,H,N,d], row-major, caller-owned and 16-byte aligned; dQ and dK
+ * include the scale), so a sequence of calls sums the contributions without rounding them to
+ * bf16 in between; fa_convert_f32_to_bf16 rounds the sums once at the end.  The additions into
+ * dk_acc and dv_acc are atomic and those into dq_acc are ordered on `stream`: calls on one
+ * stream may share accumulators; calls on other streams must not share dq_acc.
+ * workspace as for fa_bwd.  No dropout.  Errors as for fa_bwd.
+ */
+fa_status fa_bwd_accumulate(const void* q, const void* k, const void* v, const void* o,
+                            const void* dout, const float* lse,
+                            float* dq_acc, float* dk_acc, float* dv_acc,
+                            int B, int H, int N, int d, float scale, int causal,
+                            void* workspace, size_t workspace_bytes, fa_stream_t stream);
+
+/*
+ * dst[i] = src[i] rounded to bf16 (to nearest, ties to even), i < n: src fp32, dst bf16, both
+ * device pointers, 16-byte aligned.  n < 1 or a null pointer -> FA_ERR_INVALID_ARG.
+ */
+fa_status fa_convert_f32_to_bf16(const float* src, void* dst, long long n, fa_stream_t stream);
+
+/*
  * Dropout ("FlashAttention 与显存" §07: applied inside the fused kernel; §09: the mask is not
  * stored, the backward pass regenerates it from the generator state).  After the softmax each
  * probability P_ij is multiplied by Z_ij = keep_ij / q_keep:

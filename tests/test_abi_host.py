@@ -116,6 +116,23 @@ def test_withhold_hook_is_one_shot_request(lib):
     assert abi.fa_test_withhold_kv_tile(-1) == -1
 
 
+def test_accumulate_and_convert_validate_before_launching(lib):
+    def acc(**kw):
+        a = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, do=FAKE, lse=FAKE, dq=FAKE, dk=FAKE, dv=FAKE,
+                 B=1, H=1, N=128, d=64, scale=0.125, causal=0, ws=FAKE, ws_bytes=1 << 30, stream=None)
+        a.update(kw)
+        return abi.fa_bwd_accumulate(*a.values())
+    assert acc(dq=None) == abi.FA_ERR_INVALID_ARG
+    assert acc(dv=None) == abi.FA_ERR_INVALID_ARG
+    assert acc(dk=FAKE + 4) == abi.FA_ERR_MISALIGNED
+    assert acc(N=0) == abi.FA_ERR_INVALID_ARG
+    assert acc(d=96) == abi.FA_ERR_UNSUPPORTED
+    assert acc(ws_bytes=16) == abi.FA_ERR_INVALID_ARG
+    assert abi.fa_convert_f32_to_bf16(FAKE, FAKE, 0, None) == abi.FA_ERR_INVALID_ARG
+    assert abi.fa_convert_f32_to_bf16(None, FAKE, 8, None) == abi.FA_ERR_INVALID_ARG
+    assert abi.fa_convert_f32_to_bf16(FAKE + 8, FAKE, 8, None) == abi.FA_ERR_MISALIGNED
+
+
 def test_profile_hook_wants_both_events_or_neither(lib):
     assert abi.fa_profile_next_bwd_main(FAKE, None) == abi.FA_ERR_INVALID_ARG
     assert abi.fa_profile_next_bwd_main(None, FAKE) == abi.FA_ERR_INVALID_ARG
