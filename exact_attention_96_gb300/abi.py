@@ -30,6 +30,9 @@ SIGNATURES = {
     "fa_fwd_fp8": (_c_int, [_c_void_p, _c_void_p, _c_void_p, _c_int, _c_void_p, _c_void_p,
                             _c_int, _c_int, _c_int, _c_int, _c_float, _c_float, _c_float, _c_float,
                             _c_int, _c_void_p]),
+    "fa_e4m3_descale": (_c_int, [_c_void_p, ctypes.c_longlong, _c_void_p, _c_void_p]),
+    "fa_quantize_e4m3": (_c_int, [_c_void_p, _c_void_p, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
+                                  _c_void_p, _c_void_p]),
     "fa_fwd_splitkv_workspace_bytes": (_c_size_t, [_c_int] * 6),
     "fa_fwd_splitkv_num_splits": (_c_int, [_c_int] * 6),
     "fa_fwd_splitkv": (_c_int, [_c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_void_p,
@@ -113,6 +116,14 @@ def fa_fwd_fp8(q8, k8, vt8, ldv, o, lse, B, H, N, d, scale, q_descale, k_descale
                stream) -> int:
     return load().fa_fwd_fp8(q8, k8, vt8, ldv, o, lse, B, H, N, d, scale, q_descale, k_descale,
                              v_descale, int(causal), stream)
+
+
+def fa_e4m3_descale(x, n, descale, stream) -> int:
+    return load().fa_e4m3_descale(x, n, descale, stream)
+
+
+def fa_quantize_e4m3(x, out8, B, H, N, d, transpose, ld, descale, stream) -> int:
+    return load().fa_quantize_e4m3(x, out8, B, H, N, d, int(transpose), ld, descale, stream)
 
 
 def fa_fwd_splitkv_workspace_bytes(B, H, Nq, Nk, d, num_splits) -> int:

@@ -69,6 +69,43 @@ def forward_fp8(q8, k8, vt8, q_descale: float, k_descale: float, v_descale: floa
     return o, l
 
 
+def quantize_fp8(x, transpose: bool = False, ld: int | None = None, descale=None):
+    """E4M3 codes of a bf16 [B, H, N, d] tensor and its fp32 descale (a 1-element CUDA tensor):
+    descale = max|x| / 448 (fa_e4m3_descale) unless given, codes = E4M3(x / descale)
+    (fa_quantize_e4m3).  transpose=True gives the [B, H, d, ld] layout of V for forward_fp8
+    (ld defaults to N rounded up to 16)."""
+    _check_qkv(x)
+    B, H, N, d = x.shape
+    with torch.cuda.device(x.device):
+        if descale is None:
+            descale = torch.empty(1, dtype=torch.float32, device=x.device)
+            abi.check("fa_e4m3_descale", abi.fa_e4m3_descale(x.data_ptr(), x.numel(), descale.data_ptr(),
+                                                             _stream(x)))
+        if transpose:
+            ld = (N + 15) // 16 * 16 if ld is None else int(ld)
+            out = torch.empty((B, H, d, ld), dtype=torch.uint8, device=x.device)
+        else:
+            ld = 0
+            out = torch.empty((B, H, N, d), dtype=torch.uint8, device=x.device)
+        abi.check("fa_quantize_e4m3", abi.fa_quantize_e4m3(x.data_ptr(), out.data_ptr(), B, H, N, d, transpose, ld,
+                                                           descale.data_ptr(), _stream(x)))
+    return out, descale
+
+
+def forward_fp8_from_bf16(q, k, v, causal: bool = False, scale: float | None = None):
+    """The FP8 forward of bf16 inputs: each of Q, K, V is quantised on the device with its own
+    descale (quantize_fp8; V transposed), the three descales are read back (one small
+    device-to-host copy) and passed to forward_fp8.  Returns (O, LSE, (q8, k8, vt8),
+    (q_descale, k_descale, v_descale))."""
+    _check_qkv(q, k, v)
+    q8, qs = quantize_fp8(q)
+    k8, ks = quantize_fp8(k)
+    vt8, vs = quantize_fp8(v, transpose=True)
+    qs_h, ks_h, vs_h = torch.cat([qs, ks, vs]).tolist()
+    o, l = forward_fp8(q8, k8, vt8, qs_h, ks_h, vs_h, causal=causal, scale=scale)
+    return o, l, (q8, k8, vt8), (qs_h, ks_h, vs_h)
+
+
 def forward_splitkv(q, k, v, num_splits: int = 0, scale: float | None = None, out=None, lse=None,
                     workspace=None):
     """Split-KV forward (no mask): q [B,H,Nq,d] against k, v [B,H,Nk,d]; returns (O, LSE)."""

@@ -22,7 +22,7 @@ BUILD = os.path.join(PKG, "_build")
 LIBDIR = os.path.join(PKG, "lib")
 LIB = os.path.join(LIBDIR, "libfa_gb300.so")
 SOURCES = ["fa_api.cu", "fa_fwd.cu", "fa_fwd_fp8.cu", "fa_bwd.cu", "fa_bwd_d256.cu", "fa_splitkv.cu",
-           "fa_noalloc.cu", "fa_host.cu"]
+           "fa_noalloc.cu", "fa_host.cu", "fa_quant.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

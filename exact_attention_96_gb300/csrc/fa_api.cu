@@ -460,6 +460,35 @@ fa_status fa_bwd_accumulate(const void* q, const void* k, const void* v, const v
                   workspace, workspace_bytes, stream, accum);
 }
 
+fa_status fa_e4m3_descale(const void* x, long long n, float* descale, fa_stream_t stream) {
+  if (!x || !descale || n < 1) return FA_ERR_INVALID_ARG;
+  if (!aligned16(x) || (reinterpret_cast<uintptr_t>(descale) & 3u) != 0) return FA_ERR_MISALIGNED;
+  int dev = 0;
+  int* err = nullptr;
+  const fa_status st = device_setup(&dev, &err);
+  if (st != FA_OK) return st;
+  const cudaError_t e = fa::launch_e4m3_descale(static_cast<const uint16_t*>(x), n, descale,
+                                                reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : cuda_fail(e);
+}
+
+fa_status fa_quantize_e4m3(const void* x, void* out8, int B, int H, int N, int d, int transpose, int ld,
+                           const float* descale, fa_stream_t stream) {
+  if (!x || !out8 || !descale) return FA_ERR_INVALID_ARG;
+  fa_status st = check_sizes(B, H, N, d);
+  if (st != FA_OK) return st;
+  if (transpose && (ld < N || ld % 16 != 0)) return FA_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(out8) || (reinterpret_cast<uintptr_t>(descale) & 3u) != 0)
+    return FA_ERR_MISALIGNED;
+  int dev = 0;
+  int* err = nullptr;
+  if ((st = device_setup(&dev, &err)) != FA_OK) return st;
+  const cudaError_t e = fa::launch_quantize_e4m3(static_cast<const uint16_t*>(x), static_cast<uint8_t*>(out8),
+                                                 B * H, N, d, transpose != 0, ld, descale,
+                                                 reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : cuda_fail(e);
+}
+
 fa_status fa_convert_f32_to_bf16(const float* src, void* dst, long long n, fa_stream_t stream) {
   if (!src || !dst || n < 1) return FA_ERR_INVALID_ARG;
   if (!aligned16(src) || !aligned16(dst)) return FA_ERR_MISALIGNED;

@@ -135,6 +135,12 @@ cudaError_t launch_bwd_all(const BwdMaps& m, const CUtensorMap& lse2, const CUte
                            bool causal, int Np, cudaStream_t s, bool dropout = false,
                            const cudaEvent_t* main_events = nullptr);
 
+// FP8 quantisation (fa_quant.cu): descale = max|x| / 448 of n bf16 values (1 for all zeros),
+// left in device memory; E4M3 codes of x / descale, as [BH, N, d] or transposed [BH, d, ld].
+cudaError_t launch_e4m3_descale(const uint16_t* x, long long n, float* descale, cudaStream_t s);
+cudaError_t launch_quantize_e4m3(const uint16_t* x, uint8_t* out, int BH, int N, int d, bool transpose, int ld,
+                                 const float* descale, cudaStream_t s);
+
 // fp32 -> bf16 (round to nearest even), n elements, 16-byte aligned pointers.
 cudaError_t launch_f32_to_bf16(const float* src, uint16_t* dst, long long n, cudaStream_t s);
 

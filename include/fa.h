@@ -78,6 +78,25 @@ fa_status fa_fwd_fp8(const void* q8, const void* k8, const void* vt8, int ldv, v
                      float v_descale, int causal, fa_stream_t stream);
 
 /*
+ * FP8 inputs on the device (the quantisation step in front of fa_fwd_fp8).
+ * fa_e4m3_descale: descale[0] = max|x| / 448 in fp32 (1 when every element is zero) over the
+ *   n bf16 values at x; descale is a caller-owned device float (4-byte aligned), written on
+ *   `stream` (it also holds the running maximum while the call runs).
+ * fa_quantize_e4m3: E4M3 codes of x / descale[0] (the quotient in fp32, rounded to the nearest
+ *   E4M3 value with ties to the even code; magnitudes above 448 saturate to +-448), one byte
+ *   each.  x: bf16 [B,H,N,d]; transpose == 0: out8 [B,H,N,d]; transpose != 0: out8
+ *   [B,H,d,ld], element (b,h,c,j) = code of x[b,h,j,c], with ld >= N a multiple of 16 and
+ *   columns N <= j < ld written as 0 -- the transposed-V layout fa_fwd_fp8 takes.  descale is
+ *   read on the device when the kernel runs (for instance straight from fa_e4m3_descale).
+ *   Sizes as for fa_fwd (d in {64, 128, 256}); x and out8 16-byte aligned.
+ * Both are asynchronous on `stream`; argument errors as for fa_fwd (ld < N or not a multiple
+ * of 16 -> FA_ERR_INVALID_ARG).
+ */
+fa_status fa_e4m3_descale(const void* x, long long n, float* descale, fa_stream_t stream);
+fa_status fa_quantize_e4m3(const void* x, void* out8, int B, int H, int N, int d, int transpose,
+                           int ld, const float* descale, fa_stream_t stream);
+
+/*
  * Split-KV forward ("Flash Attention 原理与实践" §5.1, the decoding variant): queries attend to
  * a key/value sequence of a different length, split into key ranges processed by separate
  * CTAs; each range writes its partial output (normalised within the range) and partial

@@ -133,6 +133,20 @@ def test_accumulate_and_convert_validate_before_launching(lib):
     assert abi.fa_convert_f32_to_bf16(FAKE + 8, FAKE, 8, None) == abi.FA_ERR_MISALIGNED
 
 
+def test_fp8_quantiser_validates_before_launching(lib):
+    q = abi.fa_quantize_e4m3
+    assert q(None, FAKE, 1, 1, 16, 128, 0, 0, FAKE, None) == abi.FA_ERR_INVALID_ARG
+    assert q(FAKE, FAKE, 1, 1, 16, 128, 0, 0, None, None) == abi.FA_ERR_INVALID_ARG
+    assert q(FAKE, FAKE, 1, 1, 0, 128, 0, 0, FAKE, None) == abi.FA_ERR_INVALID_ARG
+    assert q(FAKE, FAKE, 1, 1, 16, 96, 0, 0, FAKE, None) == abi.FA_ERR_UNSUPPORTED
+    assert q(FAKE, FAKE, 1, 1, 20, 128, 1, 16, FAKE, None) == abi.FA_ERR_INVALID_ARG   # ld < N
+    assert q(FAKE, FAKE, 1, 1, 20, 128, 1, 40, FAKE, None) == abi.FA_ERR_INVALID_ARG   # ld % 16
+    assert q(FAKE + 2, FAKE, 1, 1, 16, 128, 0, 0, FAKE, None) == abi.FA_ERR_MISALIGNED
+    assert abi.fa_e4m3_descale(FAKE, 0, FAKE, None) == abi.FA_ERR_INVALID_ARG
+    assert abi.fa_e4m3_descale(FAKE, 8, None, None) == abi.FA_ERR_INVALID_ARG
+    assert abi.fa_e4m3_descale(FAKE + 8, 8, FAKE, None) == abi.FA_ERR_MISALIGNED
+
+
 def test_profile_hook_wants_both_events_or_neither(lib):
     assert abi.fa_profile_next_bwd_main(FAKE, None) == abi.FA_ERR_INVALID_ARG
     assert abi.fa_profile_next_bwd_main(None, FAKE) == abi.FA_ERR_INVALID_ARG
