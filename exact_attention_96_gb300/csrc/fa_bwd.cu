@@ -258,6 +258,8 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
   // order lost 8-11 % on the non-causal shapes, which keep the shared columns and dQ, dK, dP).
   constexpr bool kOwnDQ = D == 64 && CAUSAL;
   constexpr int kColDQ = kOwnDQ ? L::kColOwnDQ : L::kColDP;
+  // key-row column halves unrolled (see the key rows)
+  constexpr bool kUnrollHalves = D == 64 && (!CAUSAL || DROPOUT);
   extern __shared__ uint8_t smem_raw[];
   const uint32_t base = smem_addr(smem_raw);
   if (base & 1023u) {  // the 128-byte swizzle needs 1024-byte aligned tiles
@@ -515,14 +517,16 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
       // phase 1: P^T
       if (!__all_sync(0xffffffffu, mbar_wait(bar(L::kBarSFull), ph, wc))) { ok = false; break; }
       tc_fence_after_sync();
-      // For D = 128 the two 32-column halves of this warpgroup's 64 query columns run as a
-      // rolled loop (phase 2 likewise): unrolled, the key-row code crowds the instruction cache
-      // that the drain, producer and MMA warps share (measured: 4x16x8192x128 causal backward
-      // 815 -> 895 TFLOP/s).  The D = 64 kernel's code is smaller and runs faster unrolled.
+      // The two 32-column halves of this warpgroup's 64 query columns run as a rolled loop
+      // (phase 2 likewise) for D = 128 and for the causal D = 64 kernel: unrolled, the key-row
+      // code (with the diagonal tile's masking) crowds the instruction cache that the drain,
+      // producer and MMA warps share (measured: 4x16x8192x128 causal backward 815 -> 895
+      // TFLOP/s; 1x8x65536x64 causal 655 -> 715).  The non-causal D = 64 kernel, and its
+      // dropout form, are smaller and run faster unrolled (16x8x4096x64: 775 against 676).
       // P^T of each half (bf16 pairs) is kept for phase 2 in its own register array, selected
       // without run-time indexing.
       uint32_t pk0[16], pk1[16];
-#pragma unroll(D == 64 ? 2 : 1)
+#pragma unroll(kUnrollHalves ? 2 : 1)
       for (int cc = 0; cc < 64; cc += 32) {
         uint32_t r[32];
         tmem_ld32(tmem + lane_off + L::kColS + c0 + cc, r);
@@ -572,7 +576,7 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
       if (it > 0) got = got && mbar_wait(bar(L::kBarDSFree), ph ^ 1, wc);
       if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
       tc_fence_after_sync();
-#pragma unroll(D == 64 ? 2 : 1)
+#pragma unroll(kUnrollHalves ? 2 : 1)
       for (int cc = 0; cc < 64; cc += 32) {
         uint32_t r[32];
         tmem_ld32(tmem + lane_off + L::kColDP + c0 + cc, r);
