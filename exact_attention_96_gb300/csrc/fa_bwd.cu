@@ -542,15 +542,9 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
           // lv holds -LSE * log2(e): two keys' exponents in one instruction
           const float2 x = ffma2(make_float2(__uint_as_float(r[e]), __uint_as_float(r[e + 1])),
                                  make_float2(sl2, sl2), make_float2(lv[e], lv[e + 1]));
-          float p0 = ex2_approx(x.x);
-          float p1 = ex2_approx(x.y);
-          if (edge) {
-            const int qa = q0 + c0 + cc + e;
-            if (qa >= N || (CAUSAL && qa < key)) p0 = 0.f;
-            if (qa + 1 >= N || (CAUSAL && qa + 1 < key)) p1 = 0.f;
-          }
-          w[e / 2] = pack_bf16x2(p0, p1);
+          w[e / 2] = pack_bf16x2(ex2_approx(x.x), ex2_approx(x.y));
         }
+        if (edge) apply_keep_mask(w, visible_bits(q0 + c0 + cc, CAUSAL ? key : 0, N));
         if (cc == 0) {
 #pragma unroll
           for (int e = 0; e < 16; ++e) pk0[e] = w[e];
@@ -603,14 +597,9 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
           }
           // dl holds -D: dS = P (dP - D) two at a time
           const float2 ds = fmul2(make_float2(p0, p1), fadd2(make_float2(dp0, dp1), make_float2(dl[e], dl[e + 1])));
-          float ds0 = ds.x, ds1 = ds.y;
-          if (edge) {
-            const int qa = q0 + c0 + cc + e;
-            if (qa >= N) ds0 = 0.f;
-            if (qa + 1 >= N) ds1 = 0.f;
-          }
-          w[e / 2] = pack_bf16x2(ds0, ds1);
+          w[e / 2] = pack_bf16x2(ds.x, ds.y);
         }
+        if (q0 + kTile > N) apply_keep_mask(w, visible_bits(q0 + c0 + cc, 0, N));
         // dS^T row t, queries c0+cc .. c0+cc+31 -> slab `half`, 16-byte chunks cc/8 ..
 #pragma unroll
         for (int i = 0; i < 4; ++i) {

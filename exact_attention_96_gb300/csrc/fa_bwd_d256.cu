@@ -277,15 +277,9 @@ fa_bwd_d256_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
           // lse2 holds -LSE * log2(e) (stored negated by the prep kernel): two keys per instruction
           const float2 x = ffma2(make_float2(__uint_as_float(r[e]), __uint_as_float(r[e + 1])),
                                  make_float2(sl2, sl2), make_float2(lse2[e], lse2[e + 1]));
-          float p0 = ex2_approx(x.x);
-          float p1 = ex2_approx(x.y);
-          if (edge) {
-            const int qa = q0 + c0 + e;
-            if (qa >= N || (CAUSAL && qa < key)) p0 = 0.f;
-            if (qa + 1 >= N || (CAUSAL && qa + 1 < key)) p1 = 0.f;
-          }
-          w[e / 2] = pack_bf16x2(p0, p1);
+          w[e / 2] = pack_bf16x2(ex2_approx(x.x), ex2_approx(x.y));
         }
+        if (edge) apply_keep_mask(w, visible_bits(q0 + c0, CAUSAL ? key : 0, N));
         if constexpr (DROPOUT) {
           // unmasked P^T for dS in the second 16 columns; P^T * keep for the dV product
           tmem_st16(tmem + lane_off + L::kColS + c0 + 16, w);
@@ -325,14 +319,9 @@ fa_bwd_d256_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
           }
           // dvv holds -D: dS = P (dP - D) two at a time
           const float2 ds = fmul2(make_float2(p0, p1), fadd2(make_float2(dp0, dp1), make_float2(dvv[e], dvv[e + 1])));
-          float ds0 = ds.x, ds1 = ds.y;
-          if (edge) {
-            const int qa = q0 + c0 + e;
-            if (qa >= N) ds0 = 0.f;
-            if (qa + 1 >= N) ds1 = 0.f;
-          }
-          w[e / 2] = pack_bf16x2(ds0, ds1);
+          w[e / 2] = pack_bf16x2(ds.x, ds.y);
         }
+        if (q0 + kQ > N) apply_keep_mask(w, visible_bits(q0 + c0, 0, N));
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int phys = ((c0 >> 3) + i) ^ (t & 7);
