@@ -249,6 +249,7 @@ fa_status bwd_impl(const void* q, const void* k, const void* v, const void* o, c
   a.dq_accum = accum ? accum[0] : nullptr;
   a.dk_accum = accum ? accum[1] : nullptr;
   a.dv_accum = accum ? accum[2] : nullptr;
+  a.causal_group = fa::kCausalGroup;  // the d = 256 launcher sets its own
   const cudaEvent_t events[2] = {g_tl_main_events[0], g_tl_main_events[1]};
   g_tl_main_events[0] = g_tl_main_events[1] = nullptr;
   const cudaError_t e = fa::launch_bwd_all(maps, m_lse2, m_dvec, m_dk, m_dv, a, causal != 0, w.Np,

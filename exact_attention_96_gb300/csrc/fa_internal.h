@@ -32,9 +32,9 @@ constexpr int kCausalGroup = 8;
 struct RankHead {
   int rank, bh;
 };
-__device__ __forceinline__ RankHead causal_order_of(int l, int tiles, int heads) {
-  const int g0 = l / (kCausalGroup * tiles) * kCausalGroup;
-  const int gs = min(kCausalGroup, heads - g0);
+__device__ __forceinline__ RankHead causal_order_of(int l, int tiles, int heads, int group = kCausalGroup) {
+  const int g0 = l / (group * tiles) * group;
+  const int gs = min(group, heads - g0);
   const int r = l - g0 * tiles;
   return {r / gs, g0 + r % gs};
 }
@@ -130,6 +130,8 @@ struct BwdArgs {
   float* dq_accum;
   float* dk_accum;
   float* dv_accum;
+  // Heads per causal dispatch group of the d = 256 kernel (set by its launcher).
+  int causal_group;
 };
 
 struct BwdMaps {
