@@ -11,10 +11,9 @@
 // The array is FA_NOALLOC_SCRATCH_BYTES (64 MiB) on every device that loads the library
 // and stays allocated until the process exits.  Host code cannot use the array's name as a
 // device address, so the first call on each device (with that device current) looks the
-// address up with cudaGetSymbolAddress and caches it; make that first call before any
-// stream capture begins.  All calls share the one array: calls that overlap on the GPU
-// (different streams, or several host threads without ordering) race on it and give
-// undefined results.  The array keeps the previous call's contents; everything that must
+// address up with cudaGetSymbolAddress and caches it for later calls.  All calls share the
+// one array: calls that overlap on the GPU (different streams, or several host threads
+// without ordering) race on it and give undefined results.  The array keeps the previous call's contents; everything that must
 // start at zero (the dQ accumulator) is cleared by the backward pass itself on every call.
 #include <cuda_runtime.h>
 

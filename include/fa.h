@@ -234,8 +234,7 @@ fa_status fa_bwd_dropout(const void* q, const void* k, const void* v, const void
  *    fa_bwd_workspace_bytes(B,H,N,d) > FA_NOALLOC_SCRATCH_BYTES (for d = 128 that is
  *    about B*H*N <= 129,000 rows); use fa_bwd with a caller workspace beyond that.
  *  - Set-up: the first call on a device, with that device current, looks up the array's
- *    device address (cudaGetSymbolAddress) and caches it; make that first call before any
- *    stream capture starts.
+ *    device address (cudaGetSymbolAddress) and caches it for later calls.
  *  - Sharing: all calls on a device use the same array.  Calls that overlap on the GPU
  *    (other streams, unordered host threads) race on it and give undefined results.  The
  *    array keeps the last call's contents; the pass clears what must start at zero.
