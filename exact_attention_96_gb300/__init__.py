@@ -6,5 +6,5 @@ points one to one, ``attention`` wraps them for torch tensors, ``inputs`` draws 
 synthetic inputs, ``build`` compiles the library in-tree.
 """
 
-from .attention import (forward, forward_fp8, forward_splitkv, backward, workspace_bytes,  # noqa: F401
-                        step_host, status_check)
+from .attention import (forward, forward_fp8, forward_fp8_from_bf16, quantize_fp8,  # noqa: F401
+                        forward_splitkv, backward, workspace_bytes, step_host, status_check)
