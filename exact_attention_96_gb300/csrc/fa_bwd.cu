@@ -233,15 +233,12 @@ struct BwdLayout {
   static constexpr int kBytes = kMiscOff + 16;
   // TMEM columns
   static constexpr int kColS = 0;      // S^T, then P^T (bf16 pairs) packed inside it
-  static constexpr int kColDP = 128;   // dP^T (and, at D = 128, then the dQ tile)
+  static constexpr int kColDP = 128;   // dP^T, then the dQ tile
   static constexpr int kColDV = 256;
   static constexpr int kColDK = 256 + D;
-  // At D = 64 the accumulators leave 128 columns free: the causal kernel gives the dQ tile
-  // columns of its own there (see the MMA order); otherwise it shares the dP^T columns.
-  static constexpr int kColOwnDQ = 256 + 2 * D;
   static constexpr int kTmemCols = 512;
   static constexpr uint32_t kStageTx = 2 * kTileBytes + 2 * 512;
-  static_assert(256 + 2 * D <= 512 && (D != 64 || kColOwnDQ + D <= 512), "TMEM budget");
+  static_assert(256 + 2 * D <= 512, "TMEM budget");
   static_assert(kBytes <= 232448, "shared memory budget");
 };
 
@@ -253,11 +250,6 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                    const __grid_constant__ CUtensorMap tmdK, const __grid_constant__ CUtensorMap tmdV,
                    const BwdArgs args) {
   using L = BwdLayout<D, NS>;
-  // Causal, D = 64: the dQ tile in columns of its own, and dP_{i+1} issued as soon as dS_i is
-  // ready, ahead of dQ_i and dK_i (1x8x65536x64 causal backward 614 -> 664 TFLOP/s; the same
-  // order lost 8-11 % on the non-causal shapes, which keep the shared columns and dQ, dK, dP).
-  constexpr bool kOwnDQ = D == 64 && CAUSAL;
-  constexpr int kColDQ = kOwnDQ ? L::kColOwnDQ : L::kColDP;
   // key-row column halves unrolled (see the key rows)
   constexpr bool kUnrollHalves = D == 64 && (!CAUSAL || DROPOUT);
   extern __shared__ uint8_t smem_raw[];
@@ -441,19 +433,11 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
         }
         if (!mbar_wait(bar(L::kBarDSReady), ph, wc)) { ok = false; break; }
         tc_fence_after_sync();
-        if constexpr (kOwnDQ) {
-          // dP_{i+1} first (the key rows read dP_i before publishing dS_i, and its stage came
-          // with Q_{i+1}), so the key rows have it early; then dQ_i into its own columns, once
-          // the drain has read dQ_{i-1} out of them
-          if (it + 1 < n_it) issue_dp(it + 1);
-          if (it > 0 && !mbar_wait(bar(L::kBarDQDrained), ph ^ 1, wc)) { ok = false; break; }
-          tc_fence_after_sync();
-        }
         // dQ_i first, with its own completion signal, so the drain warps read it while dK_i
-        // runs and dP_{i+1}, where it reuses the dQ columns, can follow dK_i without a gap.
+        // runs and dP_{i+1} (which reuses its columns) can follow dK_i without a gap.
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk) {
-          mma_ss(tmem + kColDQ, sdesc_sw128(sdS + kk * (16 * 128), kTile * 128, 1024),
+          mma_ss(tmem + L::kColDP, sdesc_sw128(sdS + kk * (16 * 128), kTile * 128, 1024),
                  sdesc_sw128(sK + kk * (16 * 128), kTile * 128, 1024), kIdDQ, kk > 0 ? 1u : 0u);
         }
         mma_commit(bar(L::kBarDQFull));
@@ -466,9 +450,12 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
         }
         mma_commit(bar(L::kBarDSFree));
         mma_commit(bar(L::kBarQEmpty + st));
-        // dP_{i+1} overwrites the dQ_i tile (unless it has columns of its own): each product
-        // waits until the drain warps have read the dQ columns under it.
-        if (!kOwnDQ && it + 1 < n_it) {
+        // dP_{i+1} overwrites the dQ_i tile: each product waits until the drain warps have
+        // read the dQ columns under it.  (At D = 64 the accumulators leave 128 TMEM columns
+        // free.  Giving the dQ tile 64 of them, with dP_{i+1} issued ahead of dQ_i and dK_i,
+        // measured slower: 1x8x65536x64 causal 764 -> 752 TFLOP/s, 16x8x4096x64 non-causal
+        // 792 -> 710.)
+        if (it + 1 < n_it) {
           if (!mbar_wait(bar(L::kBarDQDrained + 0), ph, wc)) { ok = false; break; }
           if constexpr (D == 64) {
             issue_dp(it + 1);
@@ -678,8 +665,8 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
 #pragma unroll
       for (int h = 0; h < D / 64; ++h) {
         uint32_t a[32], b[32];
-        tmem_ld32(tmem + lane_off + kColDQ + 64 * h, a);
-        tmem_ld32(tmem + lane_off + kColDQ + 64 * h + 32, b);
+        tmem_ld32(tmem + lane_off + L::kColDP + 64 * h, a);
+        tmem_ld32(tmem + lane_off + L::kColDP + 64 * h + 32, b);
         // these 64 columns are in registers: the dP half over them may be written
         tc_fence_before_sync();
         mbar_arrive(bar(L::kBarDQDrained + h));

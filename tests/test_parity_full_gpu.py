@@ -153,3 +153,28 @@ def test_wide_head_d256_causal_fwd_bwd():
     host, o, lse, grads = run(2, 8, 16384, 256, True, seed=80)
     check_whole_heads(host, o, lse, grads, [(1, 5)], 256, True)
     check_identities(grads, host[3])
+
+
+def test_wide_head_d256_causal_dispatch_groups():
+    # The d = 256 backward dispatches causal heads in groups whose streamed tensors fit L2:
+    # two heads at N = 16384, so three heads leave a last group of one; one head from
+    # N ~ 42k on.  Both launch orders must give the same gradients as the oracle.
+    host, o, lse, grads = run(1, 3, 16384, 256, True, seed=90)
+    check_whole_heads(host, o, lse, grads, [(0, 2)], 256, True)
+    check_identities(grads, host[3])
+
+    N = 42000  # a ragged length (not a multiple of the 64-row query tile)
+    host, o, lse, grads = run(1, 2, N, 256, True, seed=91)
+    q, k, v, do = host
+    dq, dk, dv = (to_f64(g) for g in grads)
+    h = 1
+    rows = np.r_[1:33, 20000:20032, N - 32:N]
+    dq_ref, _ = A.attention_bwd_rows(head(q, 0, h), head(k, 0, h), head(v, 0, h), head(do, 0, h),
+                                     1 / 16, True, rows)
+    assert rel_fro(dq[0, h, rows], dq_ref) <= GRAD_REL_FRO
+    keys = np.r_[0:16, 21000:21016, N - 16:N]
+    dk_ref, dv_ref = A.attention_bwd_key_columns(head(q, 0, h), head(k, 0, h), head(v, 0, h),
+                                                 head(do, 0, h), 1 / 16, True, keys, row_chunk=1024)
+    assert rel_fro(dk[0, h, keys], dk_ref) <= GRAD_REL_FRO
+    assert rel_fro(dv[0, h, keys], dv_ref) <= GRAD_REL_FRO
+    check_identities(grads, do)
