@@ -290,18 +290,23 @@ fa_fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
         for (int c = 0; c < kBC; ++c)
           if (c >= lim) s[c] = -INFINITY;
       }
-      float mx0 = fmaxf(s[0], s[1]), mx1 = fmaxf(s[2], s[3]);
+      // four independent chains for the maximum and two for the sum: shorter dependency
+      // chains (4x16x8192x128 causal 1341 -> 1351 TFLOP/s; the bf16 forward measured within
+      // +-0.8 % either way and keeps two)
+      float mx0 = fmaxf(s[0], s[1]), mx1 = fmaxf(s[2], s[3]), mx2 = fmaxf(s[4], s[5]), mx3 = fmaxf(s[6], s[7]);
 #pragma unroll
-      for (int c = 4; c < kBC; c += 4) {
+      for (int c = 8; c < kBC; c += 8) {
         mx0 = fmax3(mx0, s[c], s[c + 1]);
         mx1 = fmax3(mx1, s[c + 2], s[c + 3]);
+        mx2 = fmax3(mx2, s[c + 4], s[c + 5]);
+        mx3 = fmax3(mx3, s[c + 6], s[c + 7]);
       }
-      const float m_new = fmaxf(m_run, fmaxf(mx0, mx1) * sl2);
+      const float m_new = fmaxf(m_run, fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2);
       const float alpha = ex2_approx(m_run - m_new);  // 0 on the first tile
       const bool grew = (j > 0) && (m_new > m_run);
       m_run = m_new;
       const float neg_m = kPBias - m_new;
-      float2 sum2 = make_float2(0.f, 0.f);
+      float2 sum2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
       // P_j into the first columns of S_j (all of S_j is in registers; the tensor core
       // touches this tile's S again only after P_j V_j)
       uint32_t pk[kBC / 4];
@@ -312,11 +317,12 @@ fa_fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant
         const float2 x23 = ffma2(make_float2(s[c + 2], s[c + 3]), make_float2(sl2, sl2), make_float2(neg_m, neg_m));
         const float p0 = ex2_approx(x01.x), p1 = ex2_approx(x01.y);
         const float p2 = ex2_approx(x23.x), p3 = ex2_approx(x23.y);
-        sum2 = fadd2(sum2, fadd2(make_float2(p0, p1), make_float2(p2, p3)));
+        sum2[(c >> 2) & 1] = fadd2(sum2[(c >> 2) & 1], fadd2(make_float2(p0, p1), make_float2(p2, p3)));
         pk[c / 4] = pack_e4m3x4(p0, p1, p2, p3);
       }
       tmem_st32(tcol, pk);
-      l_run = l_run * alpha + (sum2.x + sum2.y);
+      const float2 sa = fadd2(sum2[0], sum2[1]);
+      l_run = l_run * alpha + (sa.x + sa.y);
       // Rescale the accumulator when this warp's rows saw a larger maximum.  O holds
       // P_0 V_0 .. P_{j-1} V_{j-1}, all complete: S_j was issued after the last of them had
       // landed, and its commit covers them.
