@@ -46,7 +46,11 @@
 // A key-row thread needs the keep bits of its key for 64 queries.  The eight lanes holding
 // keys 8g .. 8g+7 share the generator calls of those keys: lane u draws the call of query
 // 8b + u (8 bits, one per key), the octet exchanges its 8 bytes by shuffles and each lane
-// takes its own bit column -- one call per lane per 8 queries, made before S^T is waited for.
+// takes its own bit column -- one call per lane per 8 queries, made before S^T is waited for
+// (d = 128).  At d = 64 the dQ drain warps draw the next query tile's bits instead, one call
+// per (8 keys, query), into a [key group][query] byte matrix in shared memory (two buffers);
+// a key row gathers its 64 bits from 64 bytes.  Both give the same bits: the same generator
+// call, coordinates and bit order.
 // P^T * keep goes to TMEM for the dV product (scale_keep applied to dV at the end).
 
 #include <cuda.h>
@@ -215,7 +219,11 @@ struct BwdLayout {
   static constexpr int kdSBytes = kTile * kTile * 2;
   static constexpr int kLseOff = kdSOff + kdSBytes;           // NS x 128 fp32
   static constexpr int kDOff = kLseOff + NS * 512;            // NS x 128 fp32
-  static constexpr int kBarOff = kDOff + NS * 512;
+  // D = 64: the dropout kernel's keep bits, drawn by the drain warps a tile ahead: two
+  // buffers of [16 key groups][128 queries] bytes (bit u of byte [g][q]: key 8g + u)
+  static constexpr int kBitsOff = kDOff + NS * 512;
+  static constexpr int kBitsBytes = D == 64 ? 2 * 16 * kTile : 0;
+  static constexpr int kBarOff = kBitsOff + kBitsBytes;
   static constexpr int kBarKV = 0;
   static constexpr int kBarQFull = 1;
   static constexpr int kBarQEmpty = kBarQFull + NS;
@@ -231,7 +239,9 @@ struct BwdLayout {
   static constexpr int kBarAccDone = kBarDSFree + 1;
   static constexpr int kBarEpi = kBarAccDone + 1;   // 2: one per column half
   static constexpr int kBarDrain = kBarEpi + 2;
-  static constexpr int kNumBars = kBarDrain + 1;
+  static constexpr int kBarBitsFull = kBarDrain + 1;   // 2: one per bits buffer
+  static constexpr int kBarBitsFree = kBarBitsFull + 2;  // 2
+  static constexpr int kNumBars = kBarBitsFree + 2;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kBytes = kMiscOff + 16;
   // TMEM columns
@@ -253,6 +263,11 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
                    const __grid_constant__ CUtensorMap tmdK, const __grid_constant__ CUtensorMap tmdV,
                    const BwdArgs args) {
   using L = BwdLayout<D, NS>;
+  // D = 64 with dropout: the keep bits come from the drain warps, which have the issue slots to
+  // spare, instead of 8 generator calls per tile in each key-row thread (16x8x4096x64 backward
+  // with dropout 391 -> 444 TFLOP/s).  D = 128 has no shared memory left for the 4 KB of
+  // buffers and keeps the key rows' own draws.
+  constexpr bool kBitsFromDrain = DROPOUT && D == 64;
   // key-row column halves unrolled (see the key rows)
   constexpr bool kUnrollHalves = D == 64 && (!CAUSAL || DROPOUT);
   extern __shared__ uint8_t smem_raw[];
@@ -298,6 +313,10 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
     mbar_init(bar(L::kBarEpi + 0), 128);
     mbar_init(bar(L::kBarEpi + 1), 128);
     mbar_init(bar(L::kBarDrain), 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar(L::kBarBitsFull + b), 128);         // drain warps
+      mbar_init(bar(L::kBarBitsFree + b), kRowThreads);  // key rows
+    }
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -496,7 +515,25 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
       const float* lse2 = reinterpret_cast<const float*>(smem + L::kLseOff + st * 512) + c0;
       const float* dvv = reinterpret_cast<const float*>(smem + L::kDOff + st * 512) + c0;
       uint32_t km[2] = {0u, 0u};  // dropout keep bits: bit c % 32 of word c / 32 = query q0 + c0 + c
-      if constexpr (DROPOUT) {
+      if constexpr (kBitsFromDrain) {
+        // bytes [t / 8][c0 .. c0 + 63] of this tile's matrix; bit t % 8 of each is this key's
+        const int bb = it & 1;
+        if (!__all_sync(0xffffffffu, mbar_wait(bar(L::kBarBitsFull + bb), (it >> 1) & 1, wc))) { ok = false; break; }
+        const uint4* src = reinterpret_cast<const uint4*>(smem + L::kBitsOff + bb * (16 * kTile) + (t >> 3) * kTile + c0);
+        const uint32_t u = uint32_t(t & 7);
+        uint64_t bits = 0;
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          const uint4 w = src[v];
+          const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e)  // bit u of each of the word's four bytes -> a nibble
+            bits |= uint64_t((((ws[e] >> u) & 0x01010101u) * 0x01020408u) >> 24) << (16 * v + 4 * e);
+        }
+        mbar_arrive(bar(L::kBarBitsFree + bb));
+        km[0] = uint32_t(bits);
+        km[1] = uint32_t(bits >> 32);
+      } else if constexpr (DROPOUT) {
         const uint64_t bits = dropout_key_bits<8>(args.dropout, key, q0 + c0, bh, lane);
         km[0] = uint32_t(bits);
         km[1] = uint32_t(bits >> 32);
@@ -659,8 +696,27 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
     // --------------------------------------------------------- dQ drain ----
     const int t = threadIdx.x - kDrainWarp0 * 32;   // query row within the tile = TMEM lane
     const uint32_t lane_off = uint32_t((warp & 3) * 32) << 16;
+    // D = 64 with dropout: draw the keep bits of query tile `i` for this CTA's 128 keys, query
+    // row t of the tile: byte [g][t] = keep bits of keys k0 + 8g .. k0 + 8g + 7
+    [[maybe_unused]] auto draw_bits = [&](int i) {
+      uint8_t* dst = smem + L::kBitsOff + (i & 1) * (16 * kTile) + t;
+      const uint32_t q = uint32_t((it_first + i) * kTile + t);
+#pragma unroll 4
+      for (int g = 0; g < 16; ++g)
+        dst[g * kTile] = uint8_t(dropout_keep8(args.dropout, uint32_t((k0 >> 3) + g), q, uint32_t(bh)));
+      mbar_arrive(bar(L::kBarBitsFull + (i & 1)));
+    };
+    if constexpr (kBitsFromDrain) draw_bits(0);
     for (int it = 0; it < n_it; ++it) {
       const int qt = it_first + it;
+      if constexpr (kBitsFromDrain) {
+        // the next tile's bits, into the buffer the key rows released after tile it - 1
+        if (it + 1 < n_it) {
+          if (it >= 1 && !__all_sync(0xffffffffu, mbar_wait(bar(L::kBarBitsFree + ((it + 1) & 1)), ((it - 1) >> 1) & 1, wc)))
+            break;
+          draw_bits(it + 1);
+        }
+      }
       if (!__all_sync(0xffffffffu, mbar_wait(bar(L::kBarDQFull), it & 1, wc))) break;
       tc_fence_after_sync();
       float4* dst = reinterpret_cast<float4*>(args.dq_acc + ((size_t)bh * n_q_tiles + qt) * 128 * D);
