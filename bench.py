@@ -64,7 +64,7 @@ class ClockSampler:
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, device_index: int, period_ms: int = 20):
+    def __init__(self, device_index: int, period_ms: int = 10):
         self.device_index = device_index
         self.period_ms = period_ms
         self.proc = None
