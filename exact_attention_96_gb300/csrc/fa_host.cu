@@ -9,7 +9,10 @@
 // the step costs about its kernel time plus one chunk's copies instead of the sum of the
 // three.  Each chunk is an ordinary fa_fwd / fa_bwd call on
 // B*H' = (heads in the chunk) rows of the [B*H, N, d] tensors, with pointers offset to the
-// chunk; every copy is one cudaMemcpyAsync of a contiguous range.
+// chunk; every copy is one cudaMemcpyAsync of a contiguous range.  A chunk's forward waits only
+// for its Q, K, V (dO follows them in), and its O and LSE leave as soon as the forward has
+// written them, so the first chunk's start and the last chunk's finish each carry one tensor
+// fewer of copies.
 
 #include <cuda_runtime.h>
 
@@ -30,7 +33,9 @@ constexpr int kMaxDevices = 64;
 struct HostPipe {
   cudaStream_t in = nullptr, out = nullptr, comp = nullptr;
   cudaEvent_t start = nullptr, done = nullptr;
-  cudaEvent_t loaded[kMaxChunks] = {}, computed[kMaxChunks] = {};
+  // per chunk: Q, K, V in; dO in; forward done; backward done
+  cudaEvent_t loaded[kMaxChunks] = {}, loaded_do[kMaxChunks] = {}, forwarded[kMaxChunks] = {},
+              computed[kMaxChunks] = {};
 };
 
 std::mutex g_pipe_mu;
@@ -50,6 +55,8 @@ fa_status pipe_for_device(HostPipe** out) {
       return FA_ERR_CUDA;
     for (int c = 0; c < kMaxChunks; ++c)
       if (cudaEventCreateWithFlags(&p.loaded[c], ef) != cudaSuccess ||
+          cudaEventCreateWithFlags(&p.loaded_do[c], ef) != cudaSuccess ||
+          cudaEventCreateWithFlags(&p.forwarded[c], ef) != cudaSuccess ||
           cudaEventCreateWithFlags(&p.computed[c], ef) != cudaSuccess)
         return FA_ERR_CUDA;
   }
@@ -119,21 +126,30 @@ fa_status fa_step_host(const void* q_h, const void* k_h, const void* v_h, const 
     const int hc = std::min(per, BH - h0);
     const size_t off = size_t(h0) * row, bytes = size_t(hc) * row;
     const size_t loff = size_t(h0) * lrow, lbytes = size_t(hc) * lrow;
-    // in: q, k, v, dO of the chunk
+    // in: q, k, v of the chunk, then its dO (the forward needs only the first three)
     const void* src[4] = {q_h, k_h, v_h, do_h};
     void* dst[4] = {q, k, v, dout};
-    for (int t = 0; t < 4; ++t)
+    for (int t = 0; t < 4; ++t) {
       if (cudaMemcpyAsync(atw(dst[t], off), at(src[t], off), bytes, cudaMemcpyHostToDevice, p->in) != cudaSuccess)
         return FA_ERR_CUDA;
+      if (t == 2 && cudaEventRecord(p->loaded[c], p->in) != cudaSuccess) return FA_ERR_CUDA;
+    }
+    if (cudaEventRecord(p->loaded_do[c], p->in) != cudaSuccess) return FA_ERR_CUDA;
     // kernels: forward and backward of the chunk's heads, alternating compute streams
     const cudaStream_t cs = (c & 1) ? p->comp : s;
     void* ws = atw(workspace, (c & 1) * ws_half);
-    if (cudaEventRecord(p->loaded[c], p->in) != cudaSuccess || cudaStreamWaitEvent(cs, p->loaded[c], 0) != cudaSuccess)
-      return FA_ERR_CUDA;
+    if (cudaStreamWaitEvent(cs, p->loaded[c], 0) != cudaSuccess) return FA_ERR_CUDA;
     const fa_stream_t fs = reinterpret_cast<fa_stream_t>(cs);
     if ((st = fa_fwd(at(q, off), at(k, off), at(v, off), atw(o, off), reinterpret_cast<float*>(atw(lse, loff)), 1, hc,
                      N, d, scale, causal, fs)) != FA_OK)
       return st;
+    // O and LSE leave as soon as the forward has written them
+    if (cudaEventRecord(p->forwarded[c], cs) != cudaSuccess ||
+        cudaStreamWaitEvent(p->out, p->forwarded[c], 0) != cudaSuccess ||
+        cudaMemcpyAsync(atw(o_h, off), at(o, off), bytes, cudaMemcpyDeviceToHost, p->out) != cudaSuccess ||
+        cudaMemcpyAsync(atw(lse_h, loff), at(lse, loff), lbytes, cudaMemcpyDeviceToHost, p->out) != cudaSuccess)
+      return FA_ERR_CUDA;
+    if (cudaStreamWaitEvent(cs, p->loaded_do[c], 0) != cudaSuccess) return FA_ERR_CUDA;
     if ((st = fa_bwd(at(q, off), at(k, off), at(v, off), at(o, off), at(dout, off),
                      reinterpret_cast<const float*>(at(lse, loff)), atw(dq, off), atw(dk, off), atw(dv, off), 1, hc,
                      N, d, scale, causal, ws, ws_half, fs)) != FA_OK)
@@ -141,14 +157,12 @@ fa_status fa_step_host(const void* q_h, const void* k_h, const void* v_h, const 
     if (cudaEventRecord(p->computed[c], cs) != cudaSuccess ||
         cudaStreamWaitEvent(p->out, p->computed[c], 0) != cudaSuccess)
       return FA_ERR_CUDA;
-    // out: O, LSE, dQ, dK, dV of the chunk
-    const void* rsrc[4] = {o, dq, dk, dv};
-    void* rdst[4] = {o_h, dq_h, dk_h, dv_h};
-    for (int t = 0; t < 4; ++t)
+    // out: dQ, dK, dV of the chunk
+    const void* rsrc[3] = {dq, dk, dv};
+    void* rdst[3] = {dq_h, dk_h, dv_h};
+    for (int t = 0; t < 3; ++t)
       if (cudaMemcpyAsync(atw(rdst[t], off), at(rsrc[t], off), bytes, cudaMemcpyDeviceToHost, p->out) != cudaSuccess)
         return FA_ERR_CUDA;
-    if (cudaMemcpyAsync(atw(lse_h, loff), at(lse, loff), lbytes, cudaMemcpyDeviceToHost, p->out) != cudaSuccess)
-      return FA_ERR_CUDA;
   }
   // the caller's stream completes after the last copy out (which follows every chunk's kernels)
   if (cudaEventRecord(p->done, p->out) != cudaSuccess || cudaStreamWaitEvent(s, p->done, 0) != cudaSuccess)
