@@ -35,6 +35,11 @@
 //                                          key-row warpgroup) -> TMEM [128,256)
 //   so the tensor core runs dV_i and S_{i+1} while the key rows compute dS_i, and dQ_i, dK_i
 //   while they compute P_{i+1}.
+// Persistent form (d = 64, non-causal, no dropout, at most 8 key tiles): one CTA per SM
+// walks the (key tile, head) items w = blockIdx.x + r * gridDim.x.  Item r + 1's K, V and
+// Q, dO loads start once item r's products have completed, while the key rows still read
+// dV, dK out of TMEM; its first dV product waits for that read.  dV and dK are staged in the
+// dS tile (idle between items) and stored by a drain warp.
 
 // dQ accumulator layout (fp32): [B*H][q tile][d/4][128 rows][4] -- for a fixed group of four
 // columns, the 128 rows of a tile are contiguous, so the 32 lanes of a warp adding one
@@ -241,7 +246,9 @@ struct BwdLayout {
   static constexpr int kBarDrain = kBarEpi + 2;
   static constexpr int kBarBitsFull = kBarDrain + 1;   // 2: one per bits buffer
   static constexpr int kBarBitsFree = kBarBitsFull + 2;  // 2
-  static constexpr int kNumBars = kBarBitsFree + 2;
+  static constexpr int kBarEpiRead = kBarBitsFree + 2;    // key rows have read dV, dK from TMEM
+  static constexpr int kBarStageFree = kBarEpiRead + 1;   // the stores have read the staging tiles
+  static constexpr int kNumBars = kBarStageFree + 1;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kBytes = kMiscOff + 16;
   // TMEM columns
@@ -255,7 +262,7 @@ struct BwdLayout {
   static_assert(kBytes <= 232448, "shared memory budget");
 };
 
-template <int D, int NS, bool CAUSAL, bool DROPOUT>
+template <int D, int NS, bool CAUSAL, bool DROPOUT, bool PERSIST>
 __global__ void __launch_bounds__(kMainThreads, 1)
 fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
@@ -268,6 +275,13 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
   // with dropout 391 -> 444 TFLOP/s).  D = 128 has no shared memory left for the 4 KB of
   // buffers and keeps the key rows' own draws.
   constexpr bool kBitsFromDrain = DROPOUT && D == 64;
+  // PERSIST (D = 64, non-causal, no dropout): one CTA per SM walks a list of (key tile, head)
+  // items, so that an item's K / V loads and first products overlap the previous item's dK /
+  // dV epilogue, and the CTA's set-up and teardown are paid once.  Every per-tile barrier
+  // phase then counts tiles across items (g = items done x tiles per item + tile); the
+  // per-item ones (K / V, accumulators done, epilogue) count items.
+  constexpr bool kPersist = PERSIST;
+  static_assert(!PERSIST || (D == 64 && !CAUSAL && !DROPOUT), "persistent form: d = 64, non-causal, no dropout");
   // key-row column halves unrolled (see the key rows)
   constexpr bool kUnrollHalves = D == 64 && (!CAUSAL || DROPOUT);
   extern __shared__ uint8_t smem_raw[];
@@ -282,13 +296,27 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
   const int lane = threadIdx.x & 31;
   // causal: key tile 0 (seen by every query tile) is the heaviest; heads in small groups
   const RankHead rh = CAUSAL ? causal_dispatch_order() : RankHead{int(blockIdx.x), int(blockIdx.y)};
-  const int bh = rh.bh;
-  const int kv_tile = rh.rank;
-  const int k0 = kv_tile * kTile;
+  int bh = rh.bh;
+  int kv_tile = rh.rank;
+  int k0 = kv_tile * kTile;
   const int N = args.N;
   const int n_q_tiles = (N + kTile - 1) / kTile;
   const int it_first = CAUSAL ? kv_tile : 0;  // query tiles before the diagonal see none of these keys
   const int n_it = n_q_tiles - it_first;
+  // items of this CTA: w = blockIdx.x + r * gridDim.x (persistent), else the one of the grid
+  const int n_items = kPersist ? n_q_tiles * args.BH : 1;
+  auto set_item = [&](int r) -> bool {  // false when this CTA has no r-th item
+    if constexpr (kPersist) {
+      const int w = int(blockIdx.x) + r * int(gridDim.x);
+      if (w >= n_items) return false;
+      kv_tile = w % n_q_tiles;
+      bh = w / n_q_tiles;
+      k0 = kv_tile * kTile;
+      return true;
+    } else {
+      return r == 0;
+    }
+  };
 
   auto bar = [&](int i) -> uint32_t { return base + L::kBarOff + 8u * uint32_t(i); };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
@@ -313,6 +341,10 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
     mbar_init(bar(L::kBarEpi + 0), 128);
     mbar_init(bar(L::kBarEpi + 1), 128);
     mbar_init(bar(L::kBarDrain), 1);
+    if constexpr (kPersist) {  // (in the one-item kernel these two inits alone cost 0.8 %)
+      mbar_init(bar(L::kBarEpiRead), kRowThreads);
+      mbar_init(bar(L::kBarStageFree), 1);
+    }
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar(L::kBarBitsFull + b), 128);         // drain warps
       mbar_init(bar(L::kBarBitsFree + b), kRowThreads);  // key rows
@@ -340,18 +372,25 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
       tma_prefetch_desc(&tmdO);
+      int arms[NS];
+#pragma unroll
+      for (int s = 0; s < NS; ++s) arms[s] = 0;
+      bool ok = true;
+      int kv_arms = 0;
+      for (int r = 0; ok && set_item(r); ++r) {
+      // K and V of the item, once every product of the previous one has completed
+      if (r > 0 && !mbar_wait(bar(L::kBarAccDone), (r - 1) & 1, wc)) { ok = false; break; }
       mbar_arrive_expect_tx(bar(L::kBarKV), 2 * L::kTileBytes);
       for (int s = 0; s < L::kSlabs; ++s) {
         tma_load_3d(sK + s * (kTile * 128), &tmK, bar(L::kBarKV), s * 64, k0, bh);
         tma_load_3d(sV + s * (kTile * 128), &tmV, bar(L::kBarKV), s * 64, k0, bh);
       }
-      int arms[NS];
-#pragma unroll
-      for (int s = 0; s < NS; ++s) arms[s] = 0;
-      bool ok = true;
+      ++kv_arms;
+      const int g0 = r * n_it;
       for (int it = 0; it < n_it; ++it) {
-        const int st = it % NS;
-        if (it >= NS && !mbar_wait(bar(L::kBarQEmpty + st), ((it / NS) - 1) & 1, wc)) { ok = false; break; }
+        const int gt = g0 + it;
+        const int st = gt % NS;
+        if (gt >= NS && !mbar_wait(bar(L::kBarQEmpty + st), ((gt / NS) - 1) & 1, wc)) { ok = false; break; }
         const int q0 = (it_first + it) * kTile;
         const uint32_t fb = bar(L::kBarQFull + st);
         mbar_arrive_expect_tx(fb, L::kStageTx);
@@ -363,13 +402,14 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
         tma_load_3d(base + L::kDOff + st * 512, &tmD, fb, q0, bh, 0);
         ++arms[st];
       }
+      }
       if (!ok) {
         auto drain = [&](uint32_t b, uint32_t parity) {
           for (uint64_t t0 = global_timer_ns();
                !mbar_try_wait(b, parity) && global_timer_ns() - t0 < wc.limit_ns;) {
           }
         };
-        drain(bar(L::kBarKV), 0);
+        if (kv_arms > 0) drain(bar(L::kBarKV), (kv_arms - 1) & 1);
         for (int s = 0; s < NS; ++s)
           if (arms[s] > 0) drain(bar(L::kBarQFull + s), (arms[s] - 1) & 1);
       }
@@ -424,71 +464,151 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
         }
         mma_commit(bar(L::kBarDPFull + h));
       };
-      bool ok = mbar_wait(bar(L::kBarKV), 0, wc) && issue_s(0);
-      if (ok) {
-        if constexpr (D == 64) {
-          issue_dp(0);
-        } else {
-          issue_dp_half(0, 0);
-          issue_dp_half(0, 1);
-        }
-      }
-      for (int it = 0; ok && it < n_it; ++it) {
-        const int st = it % NS;
-        const uint32_t ph = it & 1;
-        if (!mbar_wait(bar(L::kBarPReady), ph, wc)) { ok = false; break; }
-        tc_fence_after_sync();
-#pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk) {
-          // P^T of queries 16kk..16kk+15 sits in 8 columns of its half's S^T range
-          mma_ts(tmem + L::kColDV, tmem + L::kColS + (kk >> 2) * 64 + (kk & 3) * 8,
-                 sdesc_sw128(sdO(st) + kk * (16 * 128), kTile * 128, 1024), kIdAcc,
-                 (it > 0 || kk > 0) ? 1u : 0u);
-        }
-        mma_commit(bar(L::kBarDVDone));
-        // S_{i+1} overwrites P^T_i, whose only reader is the dV product (the key-row warps
-        // keep their own copy of P in registers): issue it as soon as dV_i has completed, so
-        // the tensor core runs dV_i and S_{i+1} while the key rows compute dS_i.
-        if (it + 1 < n_it && !(mbar_wait(bar(L::kBarDVDone), ph, wc) && issue_s(it + 1))) {
-          ok = false;
-          break;
-        }
-        if (!mbar_wait(bar(L::kBarDSReady), ph, wc)) { ok = false; break; }
-        tc_fence_after_sync();
-        // dQ_i first, with its own completion signal, so the drain warps read it while dK_i
-        // runs and dP_{i+1} (which reuses its columns) can follow dK_i without a gap.
-#pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk) {
-          mma_ss(tmem + L::kColDP, sdesc_sw128(sdS + kk * (16 * 128), kTile * 128, 1024),
-                 sdesc_sw128(sK + kk * (16 * 128), kTile * 128, 1024), kIdDQ, kk > 0 ? 1u : 0u);
-        }
-        mma_commit(bar(L::kBarDQFull));
-#pragma unroll
-        for (int kk = 0; kk < kTile / 16; ++kk) {
-          const uint32_t a_off = (kk >> 2) * (kTile * 128) + (kk & 3) * 32;  // dS^T K-major
-          mma_ss(tmem + L::kColDK, sdesc_sw128(sdS + a_off, 16, 1024),
-                 sdesc_sw128(sQ(st) + kk * (16 * 128), kTile * 128, 1024), kIdAcc,
-                 (it > 0 || kk > 0) ? 1u : 0u);
-        }
-        mma_commit(bar(L::kBarDSFree));
-        mma_commit(bar(L::kBarQEmpty + st));
-        // dP_{i+1} overwrites the dQ_i tile: each product waits until the drain warps have
-        // read the dQ columns under it.  (At D = 64 the accumulators leave 128 TMEM columns
-        // free.  Giving the dQ tile 64 of them, with dP_{i+1} issued ahead of dQ_i and dK_i,
-        // measured slower: 1x8x65536x64 causal 764 -> 752 TFLOP/s, 16x8x4096x64 non-causal
-        // 792 -> 710.)
-        if (it + 1 < n_it) {
-          if (!mbar_wait(bar(L::kBarDQDrained + 0), ph, wc)) { ok = false; break; }
+      if constexpr (kPersist) {
+        bool ok = true;
+        for (int r = 0; ok && set_item(r); ++r) {
+        const int g0 = r * n_it;
+        ok = mbar_wait(bar(L::kBarKV), r & 1, wc) && issue_s(g0);
+        // dP of the item's first tile overwrites the previous item's last dQ tile
+        if (ok && r > 0) ok = mbar_wait(bar(L::kBarDQDrained), (g0 - 1) & 1, wc);
+        if (ok) {
           if constexpr (D == 64) {
-            issue_dp(it + 1);
+            issue_dp(g0);
           } else {
-            issue_dp_half(it + 1, 0);
-            if (!mbar_wait(bar(L::kBarDQDrained + 1), ph, wc)) { ok = false; break; }
-            issue_dp_half(it + 1, 1);
+            issue_dp_half(g0, 0);
+            issue_dp_half(g0, 1);
           }
         }
+        for (int it = 0; ok && it < n_it; ++it) {
+          const int gt = g0 + it;
+          const int st = gt % NS;
+          const uint32_t ph = gt & 1;
+          if (!mbar_wait(bar(L::kBarPReady), ph, wc)) { ok = false; break; }
+          // the item's first dV overwrites the accumulators: the key rows must have read the
+          // previous item's out of TMEM
+          if (kPersist && it == 0 && r > 0 && !mbar_wait(bar(L::kBarEpiRead), (r - 1) & 1, wc)) { ok = false; break; }
+          tc_fence_after_sync();
+#pragma unroll
+          for (int kk = 0; kk < kTile / 16; ++kk) {
+            // P^T of queries 16kk..16kk+15 sits in 8 columns of its half's S^T range
+            mma_ts(tmem + L::kColDV, tmem + L::kColS + (kk >> 2) * 64 + (kk & 3) * 8,
+                   sdesc_sw128(sdO(st) + kk * (16 * 128), kTile * 128, 1024), kIdAcc,
+                   (it > 0 || kk > 0) ? 1u : 0u);
+          }
+          mma_commit(bar(L::kBarDVDone));
+          // S_{i+1} overwrites P^T_i, whose only reader is the dV product (the key-row warps
+          // keep their own copy of P in registers): issue it as soon as dV_i has completed, so
+          // the tensor core runs dV_i and S_{i+1} while the key rows compute dS_i.
+          if (it + 1 < n_it && !(mbar_wait(bar(L::kBarDVDone), ph, wc) && issue_s(gt + 1))) {
+            ok = false;
+            break;
+          }
+          if (!mbar_wait(bar(L::kBarDSReady), ph, wc)) { ok = false; break; }
+          tc_fence_after_sync();
+          // dQ_i first, with its own completion signal, so the drain warps read it while dK_i
+          // runs and dP_{i+1} (which reuses its columns) can follow dK_i without a gap.
+#pragma unroll
+          for (int kk = 0; kk < kTile / 16; ++kk) {
+            mma_ss(tmem + L::kColDP, sdesc_sw128(sdS + kk * (16 * 128), kTile * 128, 1024),
+                   sdesc_sw128(sK + kk * (16 * 128), kTile * 128, 1024), kIdDQ, kk > 0 ? 1u : 0u);
+          }
+          mma_commit(bar(L::kBarDQFull));
+#pragma unroll
+          for (int kk = 0; kk < kTile / 16; ++kk) {
+            const uint32_t a_off = (kk >> 2) * (kTile * 128) + (kk & 3) * 32;  // dS^T K-major
+            mma_ss(tmem + L::kColDK, sdesc_sw128(sdS + a_off, 16, 1024),
+                   sdesc_sw128(sQ(st) + kk * (16 * 128), kTile * 128, 1024), kIdAcc,
+                   (it > 0 || kk > 0) ? 1u : 0u);
+          }
+          mma_commit(bar(L::kBarDSFree));
+          mma_commit(bar(L::kBarQEmpty + st));
+          // dP_{i+1} overwrites the dQ_i tile: each product waits until the drain warps have
+          // read the dQ columns under it.  (At D = 64 the accumulators leave 128 TMEM columns
+          // free.  Giving the dQ tile 64 of them, with dP_{i+1} issued ahead of dQ_i and dK_i,
+          // measured slower: 1x8x65536x64 causal 764 -> 752 TFLOP/s, 16x8x4096x64 non-causal
+          // 792 -> 710.)
+          if (it + 1 < n_it) {
+            if (!mbar_wait(bar(L::kBarDQDrained + 0), ph, wc)) { ok = false; break; }
+            if constexpr (D == 64) {
+              issue_dp(gt + 1);
+            } else {
+              issue_dp_half(gt + 1, 0);
+              if (!mbar_wait(bar(L::kBarDQDrained + 1), ph, wc)) { ok = false; break; }
+              issue_dp_half(gt + 1, 1);
+            }
+          }
+        }
+        if (ok) mma_commit(bar(L::kBarAccDone));
+        }
+      } else {
+        // one item (an item loop around this, even one that runs once, measured 3 % slower
+        // at 16x8x4096x64: the issuing thread is on the critical path)
+        bool ok = mbar_wait(bar(L::kBarKV), 0, wc) && issue_s(0);
+        if (ok) {
+          if constexpr (D == 64) {
+            issue_dp(0);
+          } else {
+            issue_dp_half(0, 0);
+            issue_dp_half(0, 1);
+          }
+        }
+        for (int it = 0; ok && it < n_it; ++it) {
+          const int st = it % NS;
+          const uint32_t ph = it & 1;
+          if (!mbar_wait(bar(L::kBarPReady), ph, wc)) { ok = false; break; }
+          tc_fence_after_sync();
+#pragma unroll
+          for (int kk = 0; kk < kTile / 16; ++kk) {
+            // P^T of queries 16kk..16kk+15 sits in 8 columns of its half's S^T range
+            mma_ts(tmem + L::kColDV, tmem + L::kColS + (kk >> 2) * 64 + (kk & 3) * 8,
+                   sdesc_sw128(sdO(st) + kk * (16 * 128), kTile * 128, 1024), kIdAcc,
+                   (it > 0 || kk > 0) ? 1u : 0u);
+          }
+          mma_commit(bar(L::kBarDVDone));
+          // S_{i+1} overwrites P^T_i, whose only reader is the dV product (the key-row warps
+          // keep their own copy of P in registers): issue it as soon as dV_i has completed, so
+          // the tensor core runs dV_i and S_{i+1} while the key rows compute dS_i.
+          if (it + 1 < n_it && !(mbar_wait(bar(L::kBarDVDone), ph, wc) && issue_s(it + 1))) {
+            ok = false;
+            break;
+          }
+          if (!mbar_wait(bar(L::kBarDSReady), ph, wc)) { ok = false; break; }
+          tc_fence_after_sync();
+          // dQ_i first, with its own completion signal, so the drain warps read it while dK_i
+          // runs and dP_{i+1} (which reuses its columns) can follow dK_i without a gap.
+#pragma unroll
+          for (int kk = 0; kk < kTile / 16; ++kk) {
+            mma_ss(tmem + L::kColDP, sdesc_sw128(sdS + kk * (16 * 128), kTile * 128, 1024),
+                   sdesc_sw128(sK + kk * (16 * 128), kTile * 128, 1024), kIdDQ, kk > 0 ? 1u : 0u);
+          }
+          mma_commit(bar(L::kBarDQFull));
+#pragma unroll
+          for (int kk = 0; kk < kTile / 16; ++kk) {
+            const uint32_t a_off = (kk >> 2) * (kTile * 128) + (kk & 3) * 32;  // dS^T K-major
+            mma_ss(tmem + L::kColDK, sdesc_sw128(sdS + a_off, 16, 1024),
+                   sdesc_sw128(sQ(st) + kk * (16 * 128), kTile * 128, 1024), kIdAcc,
+                   (it > 0 || kk > 0) ? 1u : 0u);
+          }
+          mma_commit(bar(L::kBarDSFree));
+          mma_commit(bar(L::kBarQEmpty + st));
+          // dP_{i+1} overwrites the dQ_i tile: each product waits until the drain warps have
+          // read the dQ columns under it.  (At D = 64 the accumulators leave 128 TMEM columns
+          // free.  Giving the dQ tile 64 of them, with dP_{i+1} issued ahead of dQ_i and dK_i,
+          // measured slower: 1x8x65536x64 causal 764 -> 752 TFLOP/s, 16x8x4096x64 non-causal
+          // 792 -> 710.)
+          if (it + 1 < n_it) {
+            if (!mbar_wait(bar(L::kBarDQDrained + 0), ph, wc)) { ok = false; break; }
+            if constexpr (D == 64) {
+              issue_dp(it + 1);
+            } else {
+              issue_dp_half(it + 1, 0);
+              if (!mbar_wait(bar(L::kBarDQDrained + 1), ph, wc)) { ok = false; break; }
+              issue_dp_half(it + 1, 1);
+            }
+          }
+        }
+        if (ok) mma_commit(bar(L::kBarAccDone));
       }
-      if (ok) mma_commit(bar(L::kBarAccDone));
       mma_commit(bar(L::kBarDrain));
       for (uint64_t t0 = global_timer_ns();
            !mbar_try_wait(bar(L::kBarDrain), 0) && global_timer_ns() - t0 < wc.limit_ns;) {
@@ -504,12 +624,15 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
     const int half = threadIdx.x >> 7;     // 0 or 1
     const int c0 = half * 64;
     const uint32_t lane_off = uint32_t((warp & 3) * 32) << 16;
-    const int key = k0 + t;
     const float sl2 = args.scale_log2;
     bool ok = true;
+    for (int r = 0; ok && set_item(r); ++r) {
+    const int key = k0 + t;
+    const int g0 = r * n_it;
     for (int it = 0; it < n_it; ++it) {
-      const int st = it % NS;
-      const uint32_t ph = it & 1;
+      const int gt = g0 + it;
+      const int st = gt % NS;
+      const uint32_t ph = gt & 1;
       const int q0 = (it_first + it) * kTile;
       const bool edge = (CAUSAL && it == 0) || (q0 + kTile > N);  // any masking in this tile
       const float* lse2 = reinterpret_cast<const float*>(smem + L::kLseOff + st * 512) + c0;
@@ -594,7 +717,9 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
       mbar_arrive(bar(L::kBarPReady));
       // phase 2: dS^T = P^T (dP^T - D)
       bool got = mbar_wait(bar(L::kBarDPFull + (L::kHalves > 1 ? half : 0)), ph, wc);
-      if (it > 0) got = got && mbar_wait(bar(L::kBarDSFree), ph ^ 1, wc);
+      if (gt > 0) got = got && mbar_wait(bar(L::kBarDSFree), ph ^ 1, wc);
+      // persistent: the previous item's dV, dK stores must have read their staging in dS
+      if (kPersist && it == 0 && r > 0) got = got && mbar_wait(bar(L::kBarStageFree), (r - 1) & 1, wc);
       if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
       tc_fence_after_sync();
 #pragma unroll(kUnrollHalves ? 2 : 1)
@@ -642,10 +767,12 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
     }
     // epilogue: half 0 stores dV, half 1 stores dK (scaled), each staged in a free stage-0
     // tile and written by one TMA store per 64-column slab
-    const bool fin = ok && __all_sync(0xffffffffu, mbar_wait(bar(L::kBarAccDone), 0, wc));
+    bool fin = ok && __all_sync(0xffffffffu, mbar_wait(bar(L::kBarAccDone), r & 1, wc));
     const uint32_t col = half == 0 ? L::kColDV : L::kColDK;
     const float mul = half == 0 ? (DROPOUT ? args.dropout.scale : 1.f) : args.scale;
-    uint8_t* stage = smem + (half == 0 ? L::kQOff : L::kdOOff);
+    // the persistent kernel stages in the dS tile (free once the item's products are done):
+    // the stage-0 Q, dO tiles may already hold the next item's loads
+    uint8_t* stage = kPersist ? smem + L::kdSOff + half * L::kTileBytes : smem + (half == 0 ? L::kQOff : L::kdOOff);
     const bool accum = args.dk_accum != nullptr;
     if (fin && accum) {
       // accumulate mode: add the fp32 rows into the caller's buffers (vector atomics)
@@ -684,13 +811,19 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
       }
       fence_proxy_async_smem();
     }
+    if constexpr (kPersist) {  // dV, dK are out of TMEM: the next item's products may overwrite them
+      tc_fence_before_sync();
+      mbar_arrive(bar(L::kBarEpiRead));
+    }
     mbar_arrive(bar(L::kBarEpi + half));
-    if (t == 0 && fin && !accum && mbar_wait(bar(L::kBarEpi + half), 0, wc) && *abort_flag == 0) {
+    if (!kPersist && t == 0 && fin && !accum && mbar_wait(bar(L::kBarEpi + half), 0, wc) && *abort_flag == 0) {
       const CUtensorMap* map = half == 0 ? &tmdV : &tmdK;
       const uint32_t src = half == 0 ? sQ(0) : sdO(0);
       for (int s = 0; s < L::kSlabs; ++s) tma_store_3d(map, src + s * (kTile * 128), s * 64, k0, bh);
       bulk_commit_group();
       bulk_wait_group_read_all();  // source read: the CTA may exit
+    }
+    if (!fin) ok = false;
     }
   } else if (warp < kProducerWarp) {
     // --------------------------------------------------------- dQ drain ----
@@ -707,6 +840,9 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
       mbar_arrive(bar(L::kBarBitsFull + (i & 1)));
     };
     if constexpr (kBitsFromDrain) draw_bits(0);
+    bool dok = true;
+    for (int r = 0; dok && set_item(r); ++r) {
+    const int g0 = r * n_it;
     for (int it = 0; it < n_it; ++it) {
       const int qt = it_first + it;
       if constexpr (kBitsFromDrain) {
@@ -717,7 +853,7 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
           draw_bits(it + 1);
         }
       }
-      if (!__all_sync(0xffffffffu, mbar_wait(bar(L::kBarDQFull), it & 1, wc))) break;
+      if (!__all_sync(0xffffffffu, mbar_wait(bar(L::kBarDQFull), (g0 + it) & 1, wc))) { dok = false; break; }
       tc_fence_after_sync();
       float4* dst = reinterpret_cast<float4*>(args.dq_acc + ((size_t)bh * n_q_tiles + qt) * 128 * D);
       const bool live = qt * kTile + t < N;
@@ -742,6 +878,24 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
         }
       }
     }
+    if constexpr (kPersist) {
+      // the item's dV and dK stores from the staging tiles, once both key-row halves have
+      // written them; the staging tiles are free again when the stores have read them
+      if (warp == kDrainWarp0) {
+        if (lane == 0) {
+          const bool got = dok && mbar_wait(bar(L::kBarEpi + 0), r & 1, wc) && mbar_wait(bar(L::kBarEpi + 1), r & 1, wc);
+          if (got && args.dk_accum == nullptr && *abort_flag == 0) {
+            tma_store_3d(&tmdV, base + L::kdSOff, 0, k0, bh);
+            tma_store_3d(&tmdK, base + L::kdSOff + L::kTileBytes, 0, k0, bh);
+            bulk_commit_group();
+            bulk_wait_group_read_all();
+          }
+          mbar_arrive(bar(L::kBarStageFree));
+        }
+        __syncwarp();
+      }
+    }
+    }
   }
 
   tc_fence_before_sync();
@@ -752,15 +906,37 @@ fa_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constan
   }
 }
 
+// Sequences of at most this many key tiles take the persistent form of the d = 64
+// non-causal backward: there a CTA's set-up, K / V loads and epilogue are a large part of
+// its few query tiles (backward, TFLOP/s: 128x16x512 457 -> 517, 64x16x1024 608 -> 645).
+// Longer ones keep one CTA per item: at 16 key tiles both forms ran alike, at 32 the
+// persistent one was 2 % slower (16x8x4096: 797 -> 779), with static item lists and the
+// K / V loads of an item waiting for the previous item's products.
+constexpr int kPersistMaxTiles = 8;
+
 template <int D, int NS, bool CAUSAL>
 cudaError_t launch_main(const BwdMaps& m, const CUtensorMap& lse2, const CUtensorMap& dmap,
                         const CUtensorMap& dk, const CUtensorMap& dv, const BwdArgs& a, cudaStream_t s,
                         bool dropout) {
   using L = BwdLayout<D, NS>;
-  auto kern = dropout ? fa_bwd_main_kernel<D, NS, CAUSAL, true> : fa_bwd_main_kernel<D, NS, CAUSAL, false>;
+  constexpr bool kCanPersist = D == 64 && !CAUSAL;
+  dim3 grid((a.N + kTile - 1) / kTile, a.BH);
+  const bool persist = kCanPersist && !dropout && int(grid.x) <= kPersistMaxTiles;
+  auto kern = dropout   ? fa_bwd_main_kernel<D, NS, CAUSAL, true, false>
+              : persist ? fa_bwd_main_kernel<D, NS, CAUSAL, false, kCanPersist>
+                        : fa_bwd_main_kernel<D, NS, CAUSAL, false, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes);
   if (e != cudaSuccess) return e;
-  dim3 grid((a.N + kTile - 1) / kTile, a.BH);
+  if (persist) {  // one CTA per SM over every (key tile, head) item
+    static int sms = 0;
+    if (sms == 0) {
+      int dev = 0;
+      if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+      if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    }
+    const int items = int(grid.x * grid.y);
+    grid = dim3(unsigned(items < sms ? items : sms), 1);
+  }
   kern<<<grid, kMainThreads, L::kBytes, s>>>(m.q, m.k, m.v, m.dout, lse2, dmap, dk, dv, a);
   return cudaGetLastError();
 }

@@ -151,6 +151,22 @@ def test_causal_many_heads(B, H, N, d):
                 check_grad(g[b, h], r[b, h], (name, b, h))
 
 
+# Non-causal launches with several (key tile, head) items for every SM: each SM walks more
+# than one item, over a ragged last tile, and every head is compared with the oracle.
+@pytest.mark.parametrize("B,H,N,d", [(8, 24, 300, 64), (4, 13, 1000, 64), (3, 40, 200, 128)])
+def test_noncausal_many_items_per_sm(B, H, N, d):
+    (q, k, v, do), (o, lse, dq, dk, dv) = fwd_bwd(B, H, N, d, False, seed=B * H + N + d)
+    scale = 1 / math.sqrt(d)
+    o_ref, lse_ref = A.attention_fwd(widen(q), widen(k), widen(v), scale, False)
+    check_fwd(to_f64(o), to_f64(lse), o_ref, lse_ref, (B, H, N, d))
+    dq_ref, dk_ref, dv_ref, _ = A.attention_bwd(widen(q), widen(k), widen(v), widen(do), scale, False)
+    for name, g, r in (("dq", dq, dq_ref), ("dk", dk, dk_ref), ("dv", dv, dv_ref)):
+        g = to_f64(g)
+        for b in range(B):
+            for h in range(H):
+                check_grad(g[b, h], r[b, h], (name, b, h))
+
+
 def test_backward_workspace_reuse_is_deterministic_up_to_atomics():
     # dQ is reduced with fp32 atomics (order varies); dK, dV are bitwise reproducible.
     host, (tq, tk, tv, tdo) = device_inputs(1, 2, 384, 128, seed=3)

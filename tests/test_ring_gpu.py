@@ -67,13 +67,14 @@ def test_ring_backward_matches_oracle(B, H, N, d, world, causal):
         assert err <= 1.1 * err1 + 2e-4, (name, err, err1)
 
 
-@pytest.mark.parametrize("d", [64, 128, 256])
-def test_bwd_accumulate_adds_in_fp32(d):
+# (6, 30, 300, 64): 540 (key tile, head) items, several for every SM
+@pytest.mark.parametrize("d,B,H", [(64, 2, 2), (128, 2, 2), (256, 2, 2), (64, 6, 30)])
+def test_bwd_accumulate_adds_in_fp32(d, B, H):
     """fa_bwd_accumulate adds dQ, dK, dV (dQ and dK scaled) in fp32 into the caller's buffers:
     one call into zeros equals the oracle's gradients, and a second call adds them again."""
     build.build()
     abi.load()
-    B, H, N, causal = 2, 2, 300, d != 64
+    N, causal = 300, d != 64
     scale = 1 / math.sqrt(d)
     q, k, v, do = I.attention_inputs(B, H, N, d, seed=50 + d)
     tq, tk, tv, tdo = map(to_device, (q, k, v, do))
