@@ -153,7 +153,12 @@ def test_causal_many_heads(B, H, N, d):
 
 # Non-causal launches with several (key tile, head) items for every SM: each SM walks more
 # than one item, over a ragged last tile, and every head is compared with the oracle.
-@pytest.mark.parametrize("B,H,N,d", [(8, 24, 300, 64), (4, 13, 1000, 64), (3, 40, 200, 128)])
+# d = 64 non-causal backward launches with at most 8 key tiles walk their items in one CTA per
+# SM; (2, 80, 1024) is the last length of that form, (2, 80, 1025) the first after it; 152 and
+# 304 heads give every CTA of a 152-SM GPU the same number of items.
+@pytest.mark.parametrize("B,H,N,d", [(8, 24, 300, 64), (4, 13, 1000, 64), (3, 40, 200, 128),
+                                     (2, 80, 1024, 64), (2, 80, 1025, 64), (1, 152, 300, 64),
+                                     (2, 152, 640, 64)])
 def test_noncausal_many_items_per_sm(B, H, N, d):
     (q, k, v, do), (o, lse, dq, dk, dv) = fwd_bwd(B, H, N, d, False, seed=B * H + N + d)
     scale = 1 / math.sqrt(d)
